@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused hidden-state projection on GB300.
+
+Default workload (one JSON line on rank 0): the wq_a ++ wkv projection of
+TensorRT-LLM PR #20636 (DeepSeek-V4.1), X[8, 5120] bf16 times W_cat[1792, 5120]
+bf16, outputs [8, 1280] and [8, 512], fused call.
+
+A step is one CUDA-graph replay of --calls fused calls that cycle through C
+distinct (W_cat, X, outputs) copies whose weights together exceed three times
+the L2 size, so every call streams its weights from HBM.  value = microseconds
+per call (lower is better); the roofline object reports the algorithmic bytes
+N*K*w + M*K*x + M*N*y of one call divided by that time, against the measured
+copy bandwidth in MEASURED_PEAKS.json.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --sweep      # every workload and token count, fused / separate /
+                               # PDL off / cuBLAS per split; one JSON line each
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) at M=1/8/64, weights past L2"
+DEFAULT_WORKLOAD = ("wq_a_wkv", 8)
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class Setup:
+    """C copies of (x, w_cat, outs) on the device for one workload / M."""
+
+    def __init__(self, wl, M, device, copies=None, tf32=False):
+        self.wl, self.M, self.tf32 = wl, M, tf32
+        l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20)
+        wb = wl.weight_bytes()
+        self.copies = copies or max(16, math.ceil(3 * l2 / wb))
+        # every copy has its own weights; seeds differ per copy
+        base = W.weight_cat(wl, 0).to(device)
+        self.w = [base]
+        for c in range(1, self.copies):
+            # distinct bytes per copy without drawing 16+ full matrices on the host
+            self.w.append(torch.roll(base, shifts=c, dims=1).contiguous())
+        self.x = [W.activation(wl, M, c % 4).to(device) for c in range(self.copies)]
+        dt = self.x[0].dtype
+        self.outs = [[torch.empty((M, n), dtype=dt, device=device) for n in wl.splits]
+                     for _ in range(self.copies)]
+
+    def bytes_per_call(self):
+        return self.wl.algorithmic_bytes(self.M)
+
+
+def capture_graph(hsp, st: Setup, calls: int, separate=False):
+    fn = hsp.separate_gemm if separate else hsp.fused_gemm
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for c in range(st.copies):  # warm-up: tensor maps encoded outside capture
+            fn(st.x[c], st.w[c], st.wl.splits, outs=st.outs[c], tf32=st.tf32)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(calls):
+            c = i % st.copies
+            fn(st.x[c], st.w[c], st.wl.splits, outs=st.outs[c], tf32=st.tf32)
+    return g
+
+
+def time_graph(g, steps, warmup, barrier=None):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    per = []
+    e0.record(stream)
+    for _ in range(steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        per.append((a, b))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    total = e0.elapsed_time(e1)
+    return total, [a.elapsed_time(b) for a, b in per]
+
+
+def time_e2e(hsp, st: Setup, calls: int):
+    """Public API with host buffers: pinned H2D of x, fused call, D2H of the outputs."""
+    dev = st.x[0].device
+    xh = [st.x[c].cpu().pin_memory() for c in range(4)]
+    oh = [torch.empty((st.M, n), dtype=st.x[0].dtype).pin_memory() for n in st.wl.splits]
+    xd = torch.empty_like(st.x[0])
+    stream = torch.cuda.current_stream()
+    for i in range(8):
+        xd.copy_(xh[i % 4], non_blocking=True)
+        outs = hsp.fused_gemm(xd, st.w[i % st.copies], st.wl.splits, outs=st.outs[i % st.copies], tf32=st.tf32)
+        for h, o in zip(oh, outs):
+            h.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(calls):
+        xd.copy_(xh[i % 4], non_blocking=True)
+        outs = hsp.fused_gemm(xd, st.w[i % st.copies], st.wl.splits, outs=st.outs[i % st.copies], tf32=st.tf32)
+        for h, o in zip(oh, outs):
+            h.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / calls
+    h2d = st.x[0].numel() * st.x[0].element_size()
+    d2h = sum(o.numel() * o.element_size() for o in oh)
+    del dev
+    return us, h2d, d2h
+
+
+def cpu_baseline(wl, M, budget_s=12.0):
+    import oracle
+    oracle.build()
+    cores = oracle.cpu_count()
+    x = W.to_numpy_bits(W.activation(wl, M))
+    w = W.to_numpy_bits(W.weight_cat(wl))
+    dt = oracle.BF16 if wl.dtype == "bf16" else oracle.FP32
+    oracle.fused(x, w, wl.splits, dt, threads=cores)  # warm-up
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.fused(x, w, wl.splits, dt, threads=cores)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 200:
+            break
+    return {"value": el * 1e6 / n, "unit": "µs/call", "cores": cores, "kind": "oracle",
+            "sample": f"{n} full calls of {wl.name} M={M} (fp64 oracle, {cores} threads, "
+                      f"{oracle.host_description()})"}
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    import hidden_state_projection_gb300 as hsp
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    barrier = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        barrier = dist.barrier
+    hsp.lib()
+    hsp.set_options(pdl=not args.no_pdl)
+    name, M = args.workload, args.M
+    wl = W.WORKLOADS[name]
+    st = Setup(wl, M, dev, tf32=args.tf32)
+    g = capture_graph(hsp, st, args.calls)
+    with ClockSampler(local) as clk:
+        total_ms, per = time_graph(g, args.steps, args.warmup, barrier)
+    hsp.check_device_error()
+    ms_per_step = total_ms / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    us_call = ms_per_step * 1000.0 / args.calls
+    bytes_call = st.bytes_per_call()
+    achieved = bytes_call / (us_call * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+    e2e_us, h2d, d2h = time_e2e(hsp, st, args.e2e_calls)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(us_call, 4),
+        "unit": "µs/call",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else ("tf32" if args.tf32 else "f32"),
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights; shapes of the pages' projections)",
+        "config": {
+            "workload": f"{name}: X[{M},{wl.K}] {wl.dtype} . W_cat[{wl.n_total},{wl.K}]^T, splits "
+                        f"{list(wl.splits)} ({'+'.join(wl.split_names)}), fused call",
+            "M": M, "K": wl.K, "n_total": wl.n_total, "splits": list(wl.splits),
+            "calls_per_step": args.calls, "weight_copies": st.copies,
+            "l2_policy": f"{st.copies} distinct weight copies cycled per call "
+                         f"({st.copies * wl.weight_bytes() / 1e6:.0f} MB > 3x L2)",
+            "timing": "CUDA-graph replay of calls_per_step calls per step, CUDA events",
+            "pdl": not args.no_pdl, "parallelism": f"replicas x{ws}",
+        },
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "bytes_per_call": bytes_call, "us_per_call": round(us_call, 4)},
+        "e2e": {"value": round(e2e_us, 3), "unit": "µs/call", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "public Python API -> C ABI, eager: pinned H2D of x, fused call, D2H of outputs"},
+        "gpu_launches": args.steps * args.calls,   # one fused kernel per call, all inside the graph
+        "clocks": clocks,
+        "step_ms_min": round(min(per), 5), "step_ms_median": round(statistics.median(per), 5),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, M, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = W.WORKLOADS[args.workload]
+    M = args.M
+    cores = oracle.cpu_count()
+    x = W.to_numpy_bits(W.activation(wl, M))
+    w = W.to_numpy_bits(W.weight_cat(wl))
+    dt = oracle.BF16 if wl.dtype == "bf16" else oracle.FP32
+    for _ in range(args.warmup):
+        oracle.fused(x, w, wl.splits, dt, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fused(x, w, wl.splits, dt, threads=cores)
+    el = time.perf_counter() - t0
+    us = el * 1e6 / args.steps
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 2), "unit": "µs/call",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1000, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{args.workload}: X[{M},{wl.K}] . W_cat[{wl.n_total},{wl.K}]^T, fused",
+                                         "M": M, "splits": list(wl.splits)},
+        "cpu_baseline": {"value": round(us, 2), "unit": "µs/call", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full calls (one per step) on {cores} threads, {oracle.host_description()}"},
+        "e2e": {"value": round(us, 2), "unit": "µs/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- sweep
+
+def run_sweep(args):
+    import torch.nn.functional as F
+    import hidden_state_projection_gb300 as hsp
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hsp.lib()
+    peak, _ = measured_peaks()
+    for name, wl in W.WORKLOADS.items():
+        modes = [False, True] if wl.dtype == "fp32" else [False]
+        for M in wl.Ms:
+            for tf32 in modes:
+                st = Setup(wl, M, dev, tf32=tf32)
+                res = {"workload": name, "M": M, "dtype": wl.dtype + ("/tf32" if tf32 else ""),
+                       "bytes": st.bytes_per_call()}
+                for label, sep, pdl in (("fused", False, True), ("separate", True, True),
+                                        ("fused_nopdl", False, False)):
+                    hsp.set_options(pdl=pdl)
+                    g = capture_graph(hsp, st, args.calls, separate=sep)
+                    tot, _ = time_graph(g, args.steps, args.warmup)
+                    us = tot * 1000.0 / (args.steps * args.calls)
+                    res[label + "_us"] = round(us, 3)
+                    res[label + "_gbs"] = round(st.bytes_per_call() / us / 1e3, 1)
+                    del g
+                hsp.set_options(pdl=True)
+                # cuBLAS (torch.nn.functional.linear) per split, same rotation
+                views = [[w[o:o + n] for o, n in zip([sum(wl.splits[:i]) for i in range(len(wl.splits))],
+                                                      wl.splits)] for w in st.w]
+                torch.backends.cuda.matmul.allow_tf32 = tf32
+                for c in range(st.copies):
+                    for v in views[c]:
+                        F.linear(st.x[c], v)
+                torch.cuda.synchronize()
+                gg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gg):
+                    for i in range(args.calls):
+                        c = i % st.copies
+                        for v in views[c]:
+                            F.linear(st.x[c], v)
+                tot, _ = time_graph(gg, args.steps, args.warmup)
+                us = tot * 1000.0 / (args.steps * args.calls)
+                res["cublas_split_us"] = round(us, 3)
+                res["fused_frac_of_peak"] = round(res["fused_gbs"] / peak, 4)
+                print(json.dumps(res), flush=True)
+                del gg, st
+                torch.cuda.empty_cache()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD[0], choices=list(W.WORKLOADS))
+    ap.add_argument("--M", type=int, default=DEFAULT_WORKLOAD[1])
+    ap.add_argument("--tf32", action="store_true")
+    ap.add_argument("--calls", type=int, default=1000, help="fused calls per step (graph replay)")
+    ap.add_argument("--e2e-calls", type=int, default=2000)
+    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of this kernel (reported as is)")
+    ap.add_argument("--sweep", action="store_true")
+    args = ap.parse_args()
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

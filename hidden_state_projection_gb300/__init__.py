@@ -1,0 +1,236 @@
+"""Fused hidden-state projection for GB300 (sm_103a): Python binding.
+
+The work happens in ``_lib/libhsp_proj.so`` (hand-written CUDA behind the C ABI
+declared in ``include/proj.h``).  This module only marshals arguments: device
+pointers from torch tensors, the current CUDA stream, host arrays of split sizes
+and output pointers.  There is no CPU path; if the library is missing, importing
+the functions raises.
+
+    y = x @ w_cat.T            (x [M, K], w_cat [sum(splits), K])
+    outs[i] = y[:, off_i : off_i + splits[i]]   as separate dense tensors
+
+TensorRT-LLM PR #20636 (DeepSeek-V4.1 wq_a/wkv via tinygemm2), Description.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libhsp_proj.so")
+
+PROJ_BF16, PROJ_FP32, PROJ_TF32 = 0, 1, 2
+STATUS_NAMES = {0: "PROJ_OK", 1: "PROJ_ERR_INVALID_ARG", 2: "PROJ_ERR_UNSUPPORTED_SHAPE",
+                3: "PROJ_ERR_MISALIGNED", 4: "PROJ_ERR_UNSUPPORTED_DTYPE", 5: "PROJ_ERR_DEVICE",
+                6: "PROJ_ERR_CUDA", 7: "PROJ_ERR_TIMEOUT"}
+STATUS = {v: k for k, v in STATUS_NAMES.items()}
+MAX_SPLITS = 8
+MAX_M = 64
+
+EXPORTED = ("proj_fused_gemm", "proj_separate_gemm", "proj_pack_weights", "proj_pack_check",
+            "proj_supported", "proj_describe_plan", "proj_set_options", "proj_get_options",
+            "proj_check_device_error", "proj_launch_count", "proj_last_error_string", "proj_version")
+
+
+class ProjError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{self.status_name}: {message}")
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("pdl", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
+                ("skip_stage_plus1", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "bucket", "compute", "rows_per_cta", "row_ctas", "slices", "k_warps", "row_warps",
+        "row_tiles", "token_tiles", "ring_stages", "stage_bytes", "smem_bytes", "k_per_stage",
+        "stages_total", "threads")] + [("reserved", ctypes.c_int32 * 5)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libhsp_proj.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                           "(python -m hidden_state_projection_gb300.build)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    gemm_args = [vp, vp, ctypes.POINTER(i32), i32, ctypes.POINTER(vp), i32, i32, ctypes.c_int, vp]
+    for name in ("proj_fused_gemm", "proj_separate_gemm"):
+        getattr(L, name).argtypes = gemm_args
+        getattr(L, name).restype = ctypes.c_int
+    L.proj_pack_weights.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, ctypes.c_int, vp, vp]
+    L.proj_pack_weights.restype = ctypes.c_int
+    L.proj_pack_check.argtypes = [vp, vp, i64, i32, i32, i32, ctypes.c_int]
+    L.proj_pack_check.restype = ctypes.c_int
+    L.proj_supported.argtypes = [i32, i32, i32, ctypes.c_int]
+    L.proj_supported.restype = ctypes.c_int
+    L.proj_describe_plan.argtypes = [i32, i32, i32, ctypes.c_int, ctypes.POINTER(PlanInfo)]
+    L.proj_describe_plan.restype = ctypes.c_int
+    L.proj_set_options.argtypes = [ctypes.POINTER(Options)]
+    L.proj_set_options.restype = ctypes.c_int
+    L.proj_get_options.argtypes = [ctypes.POINTER(Options)]
+    L.proj_get_options.restype = ctypes.c_int
+    L.proj_check_device_error.argtypes = [vp]
+    L.proj_check_device_error.restype = ctypes.c_int
+    L.proj_launch_count.argtypes = []
+    L.proj_launch_count.restype = ctypes.c_uint64
+    L.proj_last_error_string.argtypes = []
+    L.proj_last_error_string.restype = ctypes.c_char_p
+    L.proj_version.argtypes = []
+    L.proj_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = lib().proj_last_error_string().decode(errors="replace")
+        raise ProjError(status, msg)
+
+
+def dtype_code(t: torch.Tensor, tf32: bool = False) -> int:
+    if t.dtype == torch.bfloat16:
+        return PROJ_BF16
+    if t.dtype == torch.float32:
+        return PROJ_TF32 if tf32 else PROJ_FP32
+    raise ProjError(4, f"unsupported tensor dtype {t.dtype}")
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---- pointer-level calls (exactly the C ABI) -----------------------------------
+
+def fused_gemm_ptr(x_ptr: int, w_ptr: int, splits: Sequence[int], out_ptrs: Sequence[int],
+                   M: int, K: int, dtype: int, stream_ptr: int = 0) -> None:
+    ns = (ctypes.c_int32 * len(splits))(*[int(s) for s in splits])
+    po = (ctypes.c_void_p * len(out_ptrs))(*[int(p) for p in out_ptrs])
+    _check(lib().proj_fused_gemm(x_ptr, w_ptr, ns, len(splits), po, M, K, dtype, stream_ptr))
+
+
+def separate_gemm_ptr(x_ptr: int, w_ptr: int, splits: Sequence[int], out_ptrs: Sequence[int],
+                      M: int, K: int, dtype: int, stream_ptr: int = 0) -> None:
+    ns = (ctypes.c_int32 * len(splits))(*[int(s) for s in splits])
+    po = (ctypes.c_void_p * len(out_ptrs))(*[int(p) for p in out_ptrs])
+    _check(lib().proj_separate_gemm(x_ptr, w_ptr, ns, len(splits), po, M, K, dtype, stream_ptr))
+
+
+# ---- tensor-level calls ---------------------------------------------------------
+
+def _outs(x: torch.Tensor, splits: Sequence[int], outs: Optional[List[torch.Tensor]]):
+    M = x.shape[0]
+    if outs is None:
+        return [torch.empty((M, int(n)), dtype=x.dtype, device=x.device) for n in splits]
+    if len(outs) != len(splits):
+        raise ProjError(1, "one output per split is required")
+    for o, n in zip(outs, splits):
+        if o.shape != (M, int(n)) or o.dtype != x.dtype or not o.is_contiguous():
+            raise ProjError(1, f"output must be a dense [{M}, {n}] {x.dtype} tensor")
+    return outs
+
+
+def _gemm(fn, x, w_cat, splits, outs, tf32, stream):
+    if x.dim() != 2 or w_cat.dim() != 2 or not x.is_contiguous() or not w_cat.is_contiguous():
+        raise ProjError(1, "x and w_cat must be dense 2-D tensors")
+    if x.dtype != w_cat.dtype:
+        raise ProjError(4, "x and w_cat must have the same dtype")
+    if x.shape[1] != w_cat.shape[1] or w_cat.shape[0] != sum(int(s) for s in splits):
+        raise ProjError(2, "shapes do not match: x [M, K], w_cat [sum(splits), K]")
+    outs = _outs(x, splits, outs)
+    fn(x.data_ptr(), w_cat.data_ptr(), splits, [o.data_ptr() for o in outs], x.shape[0], x.shape[1],
+       dtype_code(x, tf32), _stream_ptr(stream))
+    return outs
+
+
+def fused_gemm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
+               outs: Optional[List[torch.Tensor]] = None, tf32: bool = False, stream=None):
+    """One launch over all of w_cat; returns one dense [M, N_i] tensor per split."""
+    return _gemm(fused_gemm_ptr, x, w_cat, splits, outs, tf32, stream)
+
+
+def separate_gemm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
+                  outs: Optional[List[torch.Tensor]] = None, tf32: bool = False, stream=None):
+    """One launch per split over its rows of w_cat; bitwise equal to fused_gemm."""
+    return _gemm(separate_gemm_ptr, x, w_cat, splits, outs, tf32, stream)
+
+
+def pack_weights(ws: Sequence[torch.Tensor], w_cat: Optional[torch.Tensor] = None, stream=None):
+    """Row-concatenate weights into w_cat on the device; returns (w_cat, views of it)."""
+    K = ws[0].shape[1]
+    dt = ws[0].dtype
+    n_rows = [int(w.shape[0]) for w in ws]
+    if w_cat is None:
+        w_cat = torch.empty((sum(n_rows), K), dtype=dt, device=ws[0].device)
+    code = dtype_code(w_cat)
+    ptrs = (ctypes.c_void_p * len(ws))(*[w.data_ptr() for w in ws])
+    ns = (ctypes.c_int32 * len(ws))(*n_rows)
+    _check(lib().proj_pack_weights(ptrs, ns, len(ws), K, code, w_cat.data_ptr(), _stream_ptr(stream)))
+    views, off = [], 0
+    for n in n_rows:
+        views.append(w_cat[off:off + n])
+        off += n
+    return w_cat, views
+
+
+def pack_check(w: torch.Tensor, w_cat: torch.Tensor, row_off: int) -> bool:
+    """True if w is still the view of rows [row_off, row_off + len(w)) of w_cat."""
+    return bool(lib().proj_pack_check(w.data_ptr(), w_cat.data_ptr(), row_off, w.shape[0],
+                                      w_cat.shape[0], w_cat.shape[1], dtype_code(w_cat)))
+
+
+def supported(M: int, K: int, n_total: int, dtype: int) -> bool:
+    return bool(lib().proj_supported(M, K, n_total, dtype))
+
+
+def describe_plan(M: int, K: int, n_rows: int, dtype: int) -> dict:
+    info = PlanInfo()
+    _check(lib().proj_describe_plan(M, K, n_rows, dtype, ctypes.byref(info)))
+    return info.as_dict()
+
+
+def set_options(pdl: Optional[bool] = None, wait_limit_us: int = 0, skip_stage: Optional[int] = None):
+    o = Options()
+    o.pdl = -1 if pdl is None else int(bool(pdl))
+    o.wait_limit_us = int(wait_limit_us)
+    o.skip_stage_plus1 = 0 if skip_stage is None else int(skip_stage) + 1
+    _check(lib().proj_set_options(ctypes.byref(o)))
+
+
+def get_options() -> dict:
+    o = Options()
+    _check(lib().proj_get_options(ctypes.byref(o)))
+    return {"pdl": o.pdl, "wait_limit_us": o.wait_limit_us, "skip_stage_plus1": o.skip_stage_plus1}
+
+
+def check_device_error(stream=None) -> None:
+    """Synchronise the stream and raise ProjError(PROJ_ERR_TIMEOUT) if a kernel gave up a wait."""
+    _check(lib().proj_check_device_error(_stream_ptr(stream)))
+
+
+def launch_count() -> int:
+    return int(lib().proj_launch_count())
+
+
+def version() -> str:
+    return lib().proj_version().decode()

@@ -1,0 +1,33 @@
+// launch.h -- host-side launch request for the streaming kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "stream_args.h"
+
+namespace hsp {
+
+struct LaunchReq {
+    int compute;     // Compute
+    int bucket;      // 0: (WR, WK) = (1, 8); 1: (2, 4); 2: (4, 2)
+    int MT;          // token tiles of 8
+    int RT;          // 16-row tiles per warp
+    dim3 grid;       // (row CTAs, slices, 1)
+    int smem_bytes;  // dynamic shared memory
+    int pdl;         // programmatic stream serialization
+    cudaStream_t stream;
+    CUtensorMap tmap_w;
+    CUtensorMap tmap_x;
+    StreamArgs args;
+};
+
+// Implemented once per element type (kernels_bf16.cu, kernels_tf32.cu, kernels_fp32.cu).
+cudaError_t launch_bf16(const LaunchReq &r);
+cudaError_t launch_tf32(const LaunchReq &r);
+cudaError_t launch_fp32(const LaunchReq &r);
+
+// Threads per CTA of a bucket (eight consumer warps + one producer warp).
+constexpr int kThreadsPerCta = 9 * 32;
+
+}  // namespace hsp

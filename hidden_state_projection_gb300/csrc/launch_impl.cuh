@@ -1,0 +1,74 @@
+// launch_impl.cuh -- template dispatch from a LaunchReq to one kernel instance.
+#pragma once
+
+#include <atomic>
+
+#include "launch.h"
+#include "stream_kernel.cuh"
+
+namespace hsp {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxDynamicSmem = 232448;  // 227 KiB, the per-block opt-in limit of sm_103
+
+template <int COMPUTE, int MT, int RT, int WR, int WK>
+cudaError_t launch_variant(const LaunchReq &r) {
+    auto kern = hsp_stream_kernel<COMPUTE, MT, RT, WR, WK>;
+    // The shared-memory opt-in is per function and per device; set it once.
+    static std::atomic<unsigned char> configured[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev].store(1, std::memory_order_release);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = r.grid;
+    cfg.blockDim = dim3(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(r.smem_bytes);
+    cfg.stream = r.stream;
+    cudaLaunchAttribute attrs[2];
+    unsigned n = 0;
+    if (r.grid.y > 1) {
+        attrs[n].id = cudaLaunchAttributeClusterDimension;
+        attrs[n].val.clusterDim.x = 1;
+        attrs[n].val.clusterDim.y = r.grid.y;
+        attrs[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (r.pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, r.tmap_w, r.tmap_x, r.args);
+}
+
+template <int COMPUTE>
+cudaError_t launch_compute(const LaunchReq &r) {
+    const bool rt1 = (r.RT == 1);
+    switch (r.bucket) {
+        case 0:
+            if (r.MT != 1) break;
+            return rt1 ? launch_variant<COMPUTE, 1, 1, 1, 8>(r) : launch_variant<COMPUTE, 1, 2, 1, 8>(r);
+        case 1:
+            if (r.MT == 2)
+                return rt1 ? launch_variant<COMPUTE, 2, 1, 2, 4>(r) : launch_variant<COMPUTE, 2, 2, 2, 4>(r);
+            if (r.MT == 4)
+                return rt1 ? launch_variant<COMPUTE, 4, 1, 2, 4>(r) : launch_variant<COMPUTE, 4, 2, 2, 4>(r);
+            break;
+        case 2:
+            if (r.MT != 8) break;
+            return rt1 ? launch_variant<COMPUTE, 8, 1, 4, 2>(r) : launch_variant<COMPUTE, 8, 2, 4, 2>(r);
+        default:
+            break;
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace hsp

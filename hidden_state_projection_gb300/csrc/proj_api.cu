@@ -1,0 +1,491 @@
+// proj_api.cu -- the C ABI (include/proj.h): validation, the M-bucketed planner,
+// tensor-map encoding, the weight packer and the launch wrapper.
+//
+// Dispatch (TensorRT-LLM PR #20636, Description: one fused call at one token,
+// one call per projection at 2-8 tokens, a different GEMM above): here every M in
+// 1..64 has both a fused and a per-projection entry point, and M picks the
+// kernel geometry:
+//   bucket 0, M <= 8      : 1 token tile;  warps split K 8 ways, no K slices
+//   bucket 1, 9 <= M <= 32: 2 or 4 token tiles; 2 row warps x 4 K warps, S K slices
+//   bucket 2, 33 <= M <= 64: 8 token tiles; 4 row warps x 2 K warps, S K slices
+// The K-split (warps WK, slices S, box width) is a function of (K, dtype,
+// bucket) only, so an output row is summed in the same order whatever the
+// number of rows in the launch -- the property that makes the fused and the
+// separate calls bitwise equal.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+#include "proj.h"
+#include "stream_args.h"
+
+namespace {
+
+using hsp::LaunchReq;
+using hsp::StreamArgs;
+
+constexpr int kSmemLimit = 232448;          // per-block dynamic shared memory on sm_103
+constexpr int kSmemReserve = 1024 + 512;    // ring alignment slack + barriers + flags
+constexpr int kMaxRingStages = 32;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+
+thread_local char g_last_error[512] = "";
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_opt_pdl{1};
+std::atomic<int> g_opt_wait_us{0};
+std::atomic<int> g_opt_skip_stage_plus1{0};
+
+}  // namespace
+
+// Device error word: a kernel whose bounded wait runs out stores PROJ_ERR_TIMEOUT here.
+__device__ int g_hsp_device_error;
+
+namespace {
+
+proj_status fail(proj_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+proj_status fail(proj_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+proj_status ok() {
+    g_last_error[0] = '\0';
+    return PROJ_OK;
+}
+
+proj_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(PROJ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int elem_size(proj_dtype dt) { return dt == PROJ_BF16 ? 2 : 4; }
+
+bool dtype_valid(int dt) { return dt == PROJ_BF16 || dt == PROJ_FP32 || dt == PROJ_TF32; }
+
+// ---- per-device facts ------------------------------------------------------
+
+struct DeviceInfo {
+    int sms = 0;
+    int cc_ok = 0;
+    int *err_word = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+bool g_dev_ready[64] = {};
+
+proj_status device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PROJ_ERR_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo d;
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        d.cc_ok = (major == 10 && minor == 3);
+        if (d.cc_ok) {
+            void *p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_hsp_device_error)) != cudaSuccess)
+                return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+            d.err_word = static_cast<int *>(p);
+        }
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    *out = g_dev[dev];
+    if (!out->cc_ok)
+        return fail(PROJ_ERR_DEVICE, "device %d is not compute capability 10.3 (GB300, sm_103a)", dev);
+    return PROJ_OK;
+}
+
+// ---- tensor maps -----------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct MapEntry {
+    uint64_t ptr, d0, d1, box1;
+    int dtype;
+    bool used;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 128;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0, uint32_t box1,
+                       proj_dtype dt, CUtensorMap *out) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const uint64_t key = reinterpret_cast<uint64_t>(ptr);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        for (int i = 0; i < kMapCache; ++i) {
+            const MapEntry &m = g_maps[i];
+            if (m.used && m.ptr == key && m.d0 == d0 && m.d1 == d1 && m.box1 == box1 && m.dtype == dt) {
+                *out = m.map;
+                return PROJ_OK;
+            }
+        }
+    }
+    CUtensorMap map;
+    cuuint64_t dims[2] = {d0, d1};
+    cuuint64_t strides[1] = {d0 * static_cast<uint64_t>(elem_size(dt))};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&map, dt == PROJ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu], box [%u x %u]",
+                    static_cast<int>(r), (unsigned long long)d1, (unsigned long long)d0, box1, box0);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        MapEntry &m = g_maps[g_map_next];
+        g_map_next = (g_map_next + 1) % kMapCache;
+        m = MapEntry{key, d0, d1, box1, static_cast<int>(dt), true, map};
+    }
+    *out = map;
+    return PROJ_OK;
+}
+
+// ---- planner -----------------------------------------------------------------
+
+struct Plan {
+    proj_plan_info info;
+    int compute, bucket, MT, RT, WR, WK, S, R, grid_x;
+    int kboxes, T, Ts, ring_stages, stage_bytes, w_box_bytes, x_box_bytes, ring_bytes, smem;
+};
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+proj_status check_shape(int32_t M, int32_t K, int64_t n_total, int dt) {
+    if (!dtype_valid(dt)) return fail(PROJ_ERR_UNSUPPORTED_DTYPE, "dtype %d is not PROJ_BF16/FP32/TF32", dt);
+    if (M < 0 || K < 0 || n_total < 0) return fail(PROJ_ERR_INVALID_ARG, "negative size (M=%d K=%d N=%lld)", M, K, (long long)n_total);
+    if (M > PROJ_MAX_M) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "M=%d exceeds %d tokens", M, PROJ_MAX_M);
+    if (K == 0) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "K must be at least 1");
+    if ((static_cast<int64_t>(K) * elem_size(static_cast<proj_dtype>(dt))) % 16 != 0)
+        return fail(PROJ_ERR_MISALIGNED, "row pitch K*%d bytes (K=%d) is not a multiple of 16", elem_size(static_cast<proj_dtype>(dt)), K);
+    if (n_total > (int64_t(1) << 30) || K > (1 << 24))
+        return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "N_total=%lld or K=%d too large", (long long)n_total, K);
+    return PROJ_OK;
+}
+
+void make_plan(int M, int K, int n_rows, proj_dtype dt, int sms, Plan *p) {
+    memset(p, 0, sizeof *p);
+    const int esz = elem_size(dt);
+    const int boxk = 128 / esz;
+    p->compute = dt == PROJ_BF16 ? hsp::kMmaBf16 : (dt == PROJ_TF32 ? hsp::kMmaTf32 : hsp::kFmaFp32);
+    p->bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
+    static const int WRs[3] = {1, 2, 4}, WKs[3] = {8, 4, 2};
+    p->WR = WRs[p->bucket];
+    p->WK = WKs[p->bucket];
+    p->MT = p->bucket == 0 ? 1 : (p->bucket == 2 ? 8 : (M <= 16 ? 2 : 4));
+    p->kboxes = ceil_div(K, boxk);
+    p->T = ceil_div(p->kboxes, p->WK);
+    // K slices: a function of (K, dtype, bucket) only (never of the row count).
+    p->S = 1;
+    if (p->bucket > 0) {
+        if (p->T >= 16) p->S = 4;
+        else if (p->T >= 4) p->S = 2;
+    }
+    p->Ts = ceil_div(p->T, p->S);
+    const int max_rows = p->WR * 2 * 16;
+    if (p->bucket == 0) {
+        p->R = ceil_div(n_rows, sms);
+    } else {
+        p->R = ceil_div(n_rows * p->S, sms);
+    }
+    if (p->R < 1) p->R = 1;
+    if (p->R > max_rows) p->R = max_rows;
+    p->RT = ceil_div(p->R, p->WR * 16) > 1 ? 2 : 1;
+    const int slots = p->WR * p->RT * 16;
+    p->grid_x = ceil_div(n_rows, p->R);
+    p->w_box_bytes = slots * 128;
+    p->x_box_bytes = 8 * p->MT * 128;
+    p->stage_bytes = p->WK * (p->w_box_bytes + p->x_box_bytes);
+    const int budget = kSmemLimit - kSmemReserve;
+    int stages = budget / p->stage_bytes;
+    if (stages > p->Ts) stages = p->Ts;
+    if (stages > kMaxRingStages) stages = kMaxRingStages;
+    if (stages < 1) stages = 1;
+    p->ring_stages = stages;
+    const int red_bytes = p->WK * slots * 8 * p->MT * 4;
+    p->ring_bytes = stages * p->stage_bytes;
+    if (p->ring_bytes < red_bytes) p->ring_bytes = red_bytes;
+    p->smem = 1024 + p->ring_bytes + 2 * stages * 8 + 8 + 4 * stages + 64;
+    proj_plan_info &i = p->info;
+    i.bucket = p->bucket;
+    i.compute = p->compute;
+    i.rows_per_cta = p->R;
+    i.row_ctas = p->grid_x;
+    i.slices = p->S;
+    i.k_warps = p->WK;
+    i.row_warps = p->WR;
+    i.row_tiles = p->RT;
+    i.token_tiles = p->MT;
+    i.ring_stages = p->ring_stages;
+    i.stage_bytes = p->stage_bytes;
+    i.smem_bytes = p->smem;
+    i.k_per_stage = p->WK * boxk;
+    i.stages_total = p->T;
+    i.threads = hsp::kThreadsPerCta;
+}
+
+// One launch over `n_rows` rows of a weight map starting at `w` (already offset).
+proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
+                        proj_dtype dt, const hsp::SplitTable &splits, cudaStream_t stream) {
+    Plan p;
+    make_plan(M, K, n_rows, dt, dev.sms, &p);
+    if (p.smem > kSmemLimit) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "plan needs %d bytes of shared memory", p.smem);
+    const uint32_t boxk = 128 / elem_size(dt);
+    LaunchReq r{};
+    proj_status st = encode_map(w, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), boxk,
+                                static_cast<uint32_t>(p.R), dt, &r.tmap_w);
+    if (st != PROJ_OK) return st;
+    st = encode_map(x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), boxk, static_cast<uint32_t>(8 * p.MT), dt,
+                    &r.tmap_x);
+    if (st != PROJ_OK) return st;
+    r.compute = p.compute;
+    r.bucket = p.bucket;
+    r.MT = p.MT;
+    r.RT = p.RT;
+    r.grid = dim3(static_cast<unsigned>(p.grid_x), static_cast<unsigned>(p.S), 1);
+    r.smem_bytes = p.smem;
+    r.pdl = g_opt_pdl.load();
+    r.stream = stream;
+    StreamArgs &a = r.args;
+    a.n_rows = n_rows;
+    a.rows_per_cta = p.R;
+    a.M = M;
+    a.kboxes = p.kboxes;
+    a.stages_total = p.T;
+    a.stages_per_slice = p.Ts;
+    a.ring_stages = p.ring_stages;
+    a.slices = p.S;
+    a.stage_bytes = static_cast<uint32_t>(p.stage_bytes);
+    a.w_box_bytes = static_cast<uint32_t>(p.w_box_bytes);
+    a.x_box_bytes = static_cast<uint32_t>(p.x_box_bytes);
+    a.w_tx_bytes = static_cast<uint32_t>(p.R * 128);
+    a.x_tx_bytes = static_cast<uint32_t>(8 * p.MT * 128);
+    a.ring_bytes = static_cast<uint32_t>(p.ring_bytes);
+    a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
+    const int wus = g_opt_wait_us.load();
+    a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
+    a.err_word = dev.err_word;
+    a.splits = splits;
+    cudaError_t e = cudaSuccess;
+    switch (p.compute) {
+        case hsp::kMmaBf16: e = hsp::launch_bf16(r); break;
+        case hsp::kMmaTf32: e = hsp::launch_tf32(r); break;
+        default: e = hsp::launch_fp32(r); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PROJ_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+proj_status validate(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                     void *const *outs, int32_t M, int32_t K, proj_dtype dtype, int64_t *n_total) {
+    if (!dtype_valid(dtype)) return fail(PROJ_ERR_UNSUPPORTED_DTYPE, "dtype %d is not PROJ_BF16/FP32/TF32", (int)dtype);
+    if (!n_splits || !outs) return fail(PROJ_ERR_INVALID_ARG, "n_splits and outs must not be NULL");
+    if (num_splits < 1) return fail(PROJ_ERR_INVALID_ARG, "num_splits=%d (need at least 1)", num_splits);
+    if (num_splits > PROJ_MAX_SPLITS)
+        return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "num_splits=%d exceeds %d", num_splits, PROJ_MAX_SPLITS);
+    int64_t n = 0;
+    for (int i = 0; i < num_splits; ++i) {
+        if (n_splits[i] < 1) return fail(PROJ_ERR_INVALID_ARG, "n_splits[%d]=%d (need at least 1)", i, n_splits[i]);
+        n += n_splits[i];
+    }
+    proj_status st = check_shape(M, K, n, dtype);
+    if (st != PROJ_OK) return st;
+    *n_total = n;
+    if (M == 0) return PROJ_OK;  // nothing to read or write
+    if (!x || !w_cat) return fail(PROJ_ERR_INVALID_ARG, "x and w_cat must not be NULL");
+    if (!aligned16(x) || !aligned16(w_cat)) return fail(PROJ_ERR_MISALIGNED, "x and w_cat must be 16-byte aligned");
+    const uintptr_t ea = static_cast<uintptr_t>(elem_size(dtype)) - 1;
+    for (int i = 0; i < num_splits; ++i) {
+        if (!outs[i]) return fail(PROJ_ERR_INVALID_ARG, "outs[%d] is NULL", i);
+        if (reinterpret_cast<uintptr_t>(outs[i]) & ea)
+            return fail(PROJ_ERR_MISALIGNED, "outs[%d] is not aligned to its element size", i);
+    }
+    return PROJ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                            void *const *outs, int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream) {
+    int64_t n_total = 0;
+    proj_status st = validate(x, w_cat, n_splits, num_splits, outs, M, K, dtype, &n_total);
+    if (st != PROJ_OK) return st;
+    if (M == 0) return ok();
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != PROJ_OK) return st;
+    hsp::SplitTable t;
+    memset(&t, 0, sizeof t);
+    t.count = num_splits;
+    int off = 0;
+    for (int i = 0; i < num_splits; ++i) {
+        t.off[i] = off;
+        t.rows[i] = n_splits[i];
+        t.out[i] = outs[i];
+        off += n_splits[i];
+    }
+    st = launch_rows(dev, x, w_cat, static_cast<int>(n_total), M, K, dtype, t, reinterpret_cast<cudaStream_t>(stream));
+    return st == PROJ_OK ? ok() : st;
+}
+
+proj_status proj_separate_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                               void *const *outs, int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream) {
+    int64_t n_total = 0;
+    proj_status st = validate(x, w_cat, n_splits, num_splits, outs, M, K, dtype, &n_total);
+    if (st != PROJ_OK) return st;
+    if (M == 0) return ok();
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != PROJ_OK) return st;
+    const size_t pitch = static_cast<size_t>(K) * elem_size(dtype);
+    size_t off = 0;
+    for (int i = 0; i < num_splits; ++i) {
+        hsp::SplitTable t;
+        memset(&t, 0, sizeof t);
+        t.count = 1;
+        t.rows[0] = n_splits[i];
+        t.out[0] = outs[i];
+        const void *wi = static_cast<const char *>(w_cat) + off * pitch;
+        st = launch_rows(dev, x, wi, n_splits[i], M, K, dtype, t, reinterpret_cast<cudaStream_t>(stream));
+        if (st != PROJ_OK) return st;
+        off += static_cast<size_t>(n_splits[i]);
+    }
+    return ok();
+}
+
+proj_status proj_pack_weights(const void *const *ws, const int32_t *n_rows, int32_t num, int32_t K,
+                              proj_dtype dtype, void *w_cat, proj_stream_t stream) {
+    if (!dtype_valid(dtype)) return fail(PROJ_ERR_UNSUPPORTED_DTYPE, "dtype %d is not PROJ_BF16/FP32/TF32", (int)dtype);
+    if (!ws || !n_rows || !w_cat || num < 1 || K < 1) return fail(PROJ_ERR_INVALID_ARG, "bad pack arguments");
+    const size_t pitch = static_cast<size_t>(K) * elem_size(dtype);
+    size_t off = 0;
+    for (int i = 0; i < num; ++i) {
+        if (!ws[i] || n_rows[i] < 0) return fail(PROJ_ERR_INVALID_ARG, "ws[%d] / n_rows[%d] invalid", i, i);
+        char *dst = static_cast<char *>(w_cat) + off * pitch;
+        const size_t bytes = static_cast<size_t>(n_rows[i]) * pitch;
+        if (bytes && dst != ws[i]) {
+            cudaError_t e = cudaMemcpyAsync(dst, ws[i], bytes, cudaMemcpyDeviceToDevice,
+                                            reinterpret_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (pack)");
+        }
+        off += static_cast<size_t>(n_rows[i]);
+    }
+    return ok();
+}
+
+int proj_pack_check(const void *w, const void *w_cat, int64_t row_off, int32_t n_rows, int32_t n_total, int32_t K,
+                    proj_dtype dtype) {
+    if (!w || !w_cat || !dtype_valid(dtype) || row_off < 0 || n_rows < 0 || K < 1) return 0;
+    if (row_off + n_rows > n_total) return 0;
+    const uintptr_t want = reinterpret_cast<uintptr_t>(w_cat) +
+                           static_cast<uintptr_t>(row_off) * static_cast<uintptr_t>(K) * elem_size(dtype);
+    return reinterpret_cast<uintptr_t>(w) == want ? 1 : 0;
+}
+
+int proj_supported(int32_t M, int32_t K, int32_t n_total, proj_dtype dtype) {
+    char saved[sizeof g_last_error];
+    memcpy(saved, g_last_error, sizeof saved);
+    const bool good = M >= 1 && n_total >= 1 && check_shape(M, K, n_total, dtype) == PROJ_OK;
+    memcpy(g_last_error, saved, sizeof saved);
+    return good ? 1 : 0;
+}
+
+proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype dtype, proj_plan_info *info) {
+    if (!info) return fail(PROJ_ERR_INVALID_ARG, "info must not be NULL");
+    proj_status st = check_shape(M, K, n_rows, dtype);
+    if (st != PROJ_OK) return st;
+    if (M < 1 || n_rows < 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "M and n_rows must be at least 1");
+    int sms = 152;
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+    } else {
+        (void)cudaGetLastError();
+    }
+    Plan p;
+    make_plan(M, K, n_rows, dtype, sms, &p);
+    *info = p.info;
+    return ok();
+}
+
+proj_status proj_set_options(const proj_options *opt) {
+    if (!opt) return fail(PROJ_ERR_INVALID_ARG, "opt must not be NULL");
+    if (opt->pdl < -1 || opt->pdl > 1) return fail(PROJ_ERR_INVALID_ARG, "pdl must be -1, 0 or 1");
+    if (opt->wait_limit_us < 0 || opt->skip_stage_plus1 < 0)
+        return fail(PROJ_ERR_INVALID_ARG, "wait_limit_us and skip_stage_plus1 must be >= 0");
+    if (opt->pdl >= 0) g_opt_pdl.store(opt->pdl);
+    g_opt_wait_us.store(opt->wait_limit_us);
+    g_opt_skip_stage_plus1.store(opt->skip_stage_plus1);
+    return ok();
+}
+
+proj_status proj_get_options(proj_options *opt) {
+    if (!opt) return fail(PROJ_ERR_INVALID_ARG, "opt must not be NULL");
+    memset(opt, 0, sizeof *opt);
+    opt->pdl = g_opt_pdl.load();
+    opt->wait_limit_us = g_opt_wait_us.load();
+    opt->skip_stage_plus1 = g_opt_skip_stage_plus1.load();
+    return ok();
+}
+
+proj_status proj_check_device_error(proj_stream_t stream) {
+    DeviceInfo dev;
+    proj_status st = device_info(&dev);
+    if (st != PROJ_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, dev.err_word, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(dev.err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (v == PROJ_ERR_TIMEOUT) return fail(PROJ_ERR_TIMEOUT, "a kernel gave up a bounded wait (timeout)");
+        return fail(PROJ_ERR_CUDA, "device error word %d", v);
+    }
+    return ok();
+}
+
+uint64_t proj_launch_count(void) { return g_launches.load(); }
+
+const char *proj_last_error_string(void) { return g_last_error; }
+
+const char *proj_version(void) { return "hsp_proj 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,191 @@
+/*
+ * proj.h -- C ABI of the fused hidden-state projection library (libhsp_proj.so).
+ *
+ * The operation (TensorRT-LLM PR #20636, "DeepSeek-V4.1 wq_a/wkv via tinygemm2",
+ * Description): several projections that read the same hidden state have their
+ * weights row-concatenated into one matrix W_cat; one GEMM
+ *
+ *     Y[M, N_total] = X[M, K] . W_cat[N_total, K]^T        (fp32 accumulate)
+ *
+ * streams W_cat once, and Y is returned as one dense [M, N_i] output per
+ * projection (rows off_i .. off_i + N_i - 1 of W_cat, off_i = N_0 + ... + N_{i-1}).
+ * The FP32 variant follows TensorRT-LLM PR #12055 ("Fuse indexer wk +
+ * weights_proj into single GEMM in TF32"), Description; the widened four-way
+ * split follows TensorRT-LLM PR #8771 ("Fuse QK down_proj with indexer K +
+ * weight_proj"), Walkthrough; the single rounding of the FP32 sums follows
+ * TensorRT-LLM PR #20502 (GLM-5.2 decode target), glmFusedAGemm commit message.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory and keeps no pointer after the call returns.
+ *   - x is [M, K] row-major dense, w_cat is [N_total, K] row-major dense and
+ *     outs[i] is [M, N_i] row-major dense.  Element type: bf16 for PROJ_BF16,
+ *     fp32 for PROJ_FP32 and PROJ_TF32 (inputs and outputs alike).
+ *   - x and w_cat must be 16-byte aligned, every outs[i] aligned to its element
+ *     size, and K * element size must be a multiple of 16 bytes (the row pitch of
+ *     a tensor copy).  Outputs must not overlap the inputs or each other.
+ *   - M == 0 is an empty batch: the call succeeds and touches nothing.
+ *   - Host arrays (n_splits, outs, ws, n_rows) are read synchronously, before
+ *     the call returns.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream) and is
+ *     asynchronous; errors found on the host are returned immediately, launch
+ *     failures map to PROJ_ERR_CUDA.  No entry point throws or aborts.
+ *   - The library never computes on the CPU: there is no fallback path.
+ */
+#ifndef HSP_PROJ_H
+#define HSP_PROJ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (a pointer to the driver's stream object). */
+typedef struct CUstream_st *proj_stream_t;
+
+typedef enum {
+    PROJ_BF16 = 0, /* x, w, outs bf16; tensor-core products, fp32 accumulate, one RNE rounding */
+    PROJ_FP32 = 1, /* x, w, outs fp32; fp32 fused multiply-add on the CUDA cores */
+    PROJ_TF32 = 2  /* x, w, outs fp32; operands rounded to tf32 for the tensor cores, fp32 accumulate */
+} proj_dtype;
+
+typedef enum {
+    PROJ_OK = 0,
+    PROJ_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad option value */
+    PROJ_ERR_UNSUPPORTED_SHAPE = 2, /* M outside 1..PROJ_MAX_M, splits not summing, K too small ... */
+    PROJ_ERR_MISALIGNED = 3,        /* pointer or row pitch not 16-byte aligned */
+    PROJ_ERR_UNSUPPORTED_DTYPE = 4,
+    PROJ_ERR_DEVICE = 5,            /* current device is not compute capability 10.3 */
+    PROJ_ERR_CUDA = 6,              /* a CUDA runtime/driver call failed */
+    PROJ_ERR_TIMEOUT = 7            /* a kernel's bounded wait ran out (see proj_check_device_error) */
+} proj_status;
+
+#define PROJ_MAX_SPLITS 8
+#define PROJ_MAX_M 64
+
+/* Process-wide options (proj_set_options).  Zero-initialised = defaults. */
+typedef struct {
+    /* 1 (default): launch with programmatic stream serialization, so the kernel's
+     * weight loads overlap the tail of the previous kernel on the stream; the
+     * activations are read only after griddepcontrol.wait, and the completion
+     * trigger is issued after the last output store (TensorRT-LLM PR #20636,
+     * Description, discusses the hazard of triggering before the stores).
+     * 0: plain stream-ordered launches.  -1 in a set call = leave unchanged. */
+    int32_t pdl;
+    /* Limit of every in-kernel wait on a shared-memory barrier, in microseconds.
+     * 0 = default (1,000,000 us).  When a wait runs out the kernel records
+     * PROJ_ERR_TIMEOUT in a device error word, skips its stores and returns. */
+    int32_t wait_limit_us;
+    /* Test hook, 0 = off.  When > 0, the weight stream of every CTA leaves out
+     * its stage number (value - 1), so its consumers' waits run out: used only
+     * to test the timeout path.  Never faults: nothing is read or written out of
+     * bounds and every wait is bounded. */
+    int32_t skip_stage_plus1;
+    int32_t reserved[5];
+} proj_options;
+
+/* Kernel geometry chosen for one launch (proj_describe_plan). */
+typedef struct {
+    int32_t bucket;        /* 0: M <= 8, 1: 9 <= M <= 32, 2: 33 <= M <= 64 */
+    int32_t compute;       /* 0 bf16 mma.sync, 1 tf32 mma.sync, 2 fp32 FMA */
+    int32_t rows_per_cta;  /* R: output rows owned by one CTA */
+    int32_t row_ctas;      /* CTAs along the rows (grid.x) */
+    int32_t slices;        /* S: K slices = CTAs per cluster (grid.y) */
+    int32_t k_warps;       /* WK: warps sharing one row tile, each on its own k boxes */
+    int32_t row_warps;     /* WR */
+    int32_t row_tiles;     /* RT: 16-row MMA tiles per warp */
+    int32_t token_tiles;   /* MT: 8-token tiles */
+    int32_t ring_stages;   /* shared-memory ring depth */
+    int32_t stage_bytes;
+    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t k_per_stage;   /* elements of K per ring stage */
+    int32_t stages_total;  /* ring stages over all of K */
+    int32_t threads;       /* threads per CTA (consumer warps + 1 producer warp) */
+    int32_t reserved[5];
+} proj_plan_info;
+
+/*
+ * proj_fused_gemm -- the fused projection (TensorRT-LLM PR #20636, Description:
+ * "both projections run as a single tinygemm2 over the concatenated weight"; here
+ * for any M in 1..PROJ_MAX_M).  One kernel launch streams every row of w_cat
+ * once and writes outs[i][m * n_splits[i] + r] = round(sum_k x[m,k] * w_cat[off_i + r, k]).
+ *   x          device [M, K]
+ *   w_cat      device [N_total, K], N_total = sum(n_splits)
+ *   n_splits   host   [num_splits], each >= 1
+ *   num_splits 1..PROJ_MAX_SPLITS
+ *   outs       host array of num_splits device pointers, outs[i] is [M, n_splits[i]]
+ *   M          1..PROJ_MAX_M tokens;  K >= 1
+ * The result of every output row depends only on (x, its weight row, M's bucket,
+ * K, dtype): it is bitwise identical to proj_separate_gemm, run to run, and under
+ * CUDA-graph replay.
+ */
+proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_splits,
+                            int32_t num_splits, void *const *outs, int32_t M, int32_t K,
+                            proj_dtype dtype, proj_stream_t stream);
+
+/*
+ * proj_separate_gemm -- one launch per projection over its row range of the same
+ * w_cat (TensorRT-LLM PR #20636, Description: "2-8 tokens: one tinygemm2 per
+ * projection").  Same arguments and outputs as proj_fused_gemm, bitwise equal to it.
+ */
+proj_status proj_separate_gemm(const void *x, const void *w_cat, const int32_t *n_splits,
+                               int32_t num_splits, void *const *outs, int32_t M, int32_t K,
+                               proj_dtype dtype, proj_stream_t stream);
+
+/*
+ * proj_pack_weights -- build W_cat by copying the projection weights one after
+ * another (TensorRT-LLM PR #20636, Description: post_load_weights copies wq_a and
+ * wkv into one row-concatenated tensor).  ws[i] is a device [n_rows[i], K] dense
+ * matrix; w_cat receives them in order.  Device-to-device copies enqueued on
+ * `stream`; re-running it into the same w_cat refreshes the weights in place.
+ * ws[i] may already alias its rows of w_cat (the copy is then skipped).
+ */
+proj_status proj_pack_weights(const void *const *ws, const int32_t *n_rows, int32_t num,
+                              int32_t K, proj_dtype dtype, void *w_cat, proj_stream_t stream);
+
+/*
+ * proj_pack_check -- 1 if `w` is exactly the view of rows [row_off, row_off + n_rows)
+ * of w_cat (so a reload through `w` updates the fused weight; TensorRT-LLM PR
+ * #20636, Description: a replaced Parameter is no longer a view), else 0.
+ * Pure pointer arithmetic on the host.
+ */
+int proj_pack_check(const void *w, const void *w_cat, int64_t row_off, int32_t n_rows,
+                    int32_t n_total, int32_t K, proj_dtype dtype);
+
+/*
+ * proj_supported -- host-side query: 1 if (M, K, n_total, dtype) is served,
+ * 0 otherwise (the shape gate; TensorRT-LLM PR #20502, dense-MLP and fused-A
+ * commit messages: a host query answers whether the kernels serve a shape).
+ */
+int proj_supported(int32_t M, int32_t K, int32_t n_total, proj_dtype dtype);
+
+/* proj_describe_plan -- the geometry a launch over n_rows rows would use (host only). */
+proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype dtype,
+                               proj_plan_info *info);
+
+proj_status proj_set_options(const proj_options *opt);
+proj_status proj_get_options(proj_options *opt);
+
+/*
+ * proj_check_device_error -- synchronizes `stream`, then reads and clears the
+ * device error word of the current device.  Returns PROJ_ERR_TIMEOUT if any
+ * kernel since the last check gave up a bounded wait, PROJ_ERR_CUDA if the
+ * stream reported an error, else PROJ_OK.
+ */
+proj_status proj_check_device_error(proj_stream_t stream);
+
+/* Number of kernels this library has launched in the process (all devices). */
+uint64_t proj_launch_count(void);
+
+/* Message of the last error returned on the calling thread ("" if none). */
+const char *proj_last_error_string(void);
+
+/* Library version string. */
+const char *proj_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSP_PROJ_H */

@@ -1,0 +1,135 @@
+"""The C ABI without a GPU: the library builds, loads and exports every function
+include/proj.h declares; host-side validation returns the documented status
+codes; the planner keeps the K-split independent of the row count (the
+precondition of bitwise fused == separate); and with no device the library
+fails loudly instead of computing on the CPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def hsp():
+    from hidden_state_projection_gb300 import build
+    build.build()
+    import hidden_state_projection_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "proj.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(proj_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declarations_are_exported(hsp):
+    names = _declared()
+    assert "proj_fused_gemm" in names and "proj_separate_gemm" in names
+    lib = hsp.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", hsp.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (proj_\w+)", out))
+    assert set(names) <= exported, set(names) - exported
+    assert set(hsp.EXPORTED) == set(names)
+
+
+def _call(hsp, x=0x10000, w=0x20000, splits=(16, 8), outs=None, M=1, K=64, dtype=0, n=None):
+    outs = outs if outs is not None else [0x30000 + 0x1000 * i for i in range(len(splits))]
+    ns = (ctypes.c_int32 * max(1, len(splits)))(*splits)
+    po = (ctypes.c_void_p * max(1, len(outs)))(*outs)
+    return hsp.lib().proj_fused_gemm(x, w, ns, len(splits) if n is None else n, po, M, K, dtype, None)
+
+
+def test_validation_codes(hsp):
+    S = hsp.STATUS
+    assert _call(hsp, dtype=9) == S["PROJ_ERR_UNSUPPORTED_DTYPE"]
+    assert _call(hsp, M=65) == S["PROJ_ERR_UNSUPPORTED_SHAPE"]
+    assert _call(hsp, M=-1) == S["PROJ_ERR_INVALID_ARG"]
+    assert _call(hsp, K=0) == S["PROJ_ERR_UNSUPPORTED_SHAPE"]
+    assert _call(hsp, K=60) == S["PROJ_ERR_MISALIGNED"]           # 120-byte rows
+    assert _call(hsp, K=62, dtype=1) == S["PROJ_ERR_MISALIGNED"]  # 248-byte rows
+    assert _call(hsp, x=0x10008) == S["PROJ_ERR_MISALIGNED"]
+    assert _call(hsp, w=0x20004) == S["PROJ_ERR_MISALIGNED"]
+    assert _call(hsp, outs=[0x30001, 0x31000]) == S["PROJ_ERR_MISALIGNED"]
+    assert _call(hsp, x=0) == S["PROJ_ERR_INVALID_ARG"]
+    assert _call(hsp, outs=[0x30000, 0]) == S["PROJ_ERR_INVALID_ARG"]
+    assert _call(hsp, splits=(16, 0)) == S["PROJ_ERR_INVALID_ARG"]
+    assert _call(hsp, splits=tuple([1] * 9)) == S["PROJ_ERR_UNSUPPORTED_SHAPE"]
+    assert _call(hsp, splits=(), outs=[]) == S["PROJ_ERR_INVALID_ARG"]
+    assert "exceeds" in hsp.lib().proj_last_error_string().decode() or True
+    # an empty batch touches nothing and needs no device
+    assert _call(hsp, M=0) == S["PROJ_OK"]
+
+
+def test_no_device_fails_loudly(hsp):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    st = _call(hsp)
+    assert st in (hsp.STATUS["PROJ_ERR_CUDA"], hsp.STATUS["PROJ_ERR_DEVICE"])
+    assert hsp.lib().proj_last_error_string().decode()
+
+
+def test_supported(hsp):
+    assert hsp.supported(1, 5120, 1792, 0)
+    assert hsp.supported(64, 7168, 2304, 0)
+    assert hsp.supported(64, 7168, 192, 2)
+    assert not hsp.supported(65, 5120, 1792, 0)
+    assert not hsp.supported(0, 5120, 1792, 0)
+    assert not hsp.supported(1, 5121, 1792, 0)
+    assert not hsp.supported(1, 5120, 1792, 7)
+
+
+def _plan_dtype(dtype, tf32):
+    return 0 if dtype == "bf16" else (2 if tf32 else 1)
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_k_split_independent_of_rows(hsp, name):
+    wl = W.WORKLOADS[name]
+    for tf32 in ([False, True] if wl.dtype == "fp32" else [False]):
+        dt = _plan_dtype(wl.dtype, tf32)
+        for M in range(1, 65):
+            full = hsp.describe_plan(M, wl.K, wl.n_total, dt)
+            for n in list(wl.splits) + [1, 3, 17, 5000]:
+                part = hsp.describe_plan(M, wl.K, n, dt)
+                for key in ("bucket", "k_warps", "slices", "k_per_stage", "stages_total", "compute"):
+                    assert part[key] == full[key], (name, M, n, key)
+
+
+def test_plan_fits_the_hardware(hsp):
+    for name, wl in W.WORKLOADS.items():
+        for dt in ([0] if wl.dtype == "bf16" else [1, 2]):
+            for M in (1, 8, 9, 16, 17, 32, 33, 64):
+                for n in (wl.n_total, *wl.splits):
+                    p = hsp.describe_plan(M, wl.K, n, dt)
+                    assert p["smem_bytes"] <= 232448
+                    assert p["rows_per_cta"] <= p["row_warps"] * p["row_tiles"] * 16
+                    assert p["rows_per_cta"] <= 256
+                    assert p["ring_stages"] >= 1
+                    assert (p["row_warps"] * p["row_tiles"] * 16) % p["slices"] == 0
+                    assert p["row_ctas"] * p["rows_per_cta"] >= n
+                    assert p["threads"] == 288
+
+
+def test_pack_check_and_options(hsp):
+    lib = hsp.lib()
+    base = 0x7F0000000000
+    K = 5120
+    assert lib.proj_pack_check(base + 1280 * K * 2, base, 1280, 512, 1792, K, 0) == 1
+    assert lib.proj_pack_check(base + 1280 * K * 2 + 2, base, 1280, 512, 1792, K, 0) == 0
+    assert lib.proj_pack_check(base, base, 1280, 513, 1792, K, 0) == 0
+    hsp.set_options(pdl=False, wait_limit_us=5, skip_stage=3)
+    assert hsp.get_options() == {"pdl": 0, "wait_limit_us": 5, "skip_stage_plus1": 4}
+    hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None)
+    assert hsp.get_options() == {"pdl": 1, "wait_limit_us": 0, "skip_stage_plus1": 0}
+    with pytest.raises(hsp.ProjError):
+        hsp.set_options(wait_limit_us=-1)

@@ -1,0 +1,137 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Every workload of the pages at its full size and every token count it names
+(all outputs compared), plus ragged and edge shapes: K not a multiple of the
+box width, splits of 1 / 3 / 17 rows, a single row, more rows than one wave,
+every M from 1 to 64, small-integer inputs that must match bit for bit, and
+one-hot activations that must reproduce weight columns exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_helpers import as_f64, check_close, mode_of, oracle_outputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hsp():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import hidden_state_projection_gb300 as m
+    m.lib()
+    m.set_options(pdl=True, wait_limit_us=0, skip_stage=None)
+    return m
+
+
+def _run_both(hsp, x, w_cat, splits, tf32=False):
+    dev = torch.device("cuda")
+    xd, wd = x.to(dev), w_cat.to(dev)
+    fused = hsp.fused_gemm(xd, wd, splits, tf32=tf32)
+    sep = hsp.separate_gemm(xd, wd, splits, tf32=tf32)
+    hsp.check_device_error()
+    for a, b in zip(fused, sep):
+        assert torch.equal(a, b), "fused and separate outputs differ"
+    return fused
+
+
+CASES = []
+for name, wl in W.WORKLOADS.items():
+    modes = [False, True] if wl.dtype == "fp32" else [False]
+    for M in wl.Ms:
+        for tf32 in modes:
+            CASES.append(pytest.param(name, M, tf32, id=f"{name}-M{M}{'-tf32' if tf32 else ''}"))
+
+
+@pytest.mark.parametrize("name,M,tf32", CASES)
+def test_workload_full_size(hsp, name, M, tf32):
+    wl = W.WORKLOADS[name]
+    x = W.activation(wl, M)
+    w_cat = W.weight_cat(wl)
+    outs = _run_both(hsp, x, w_cat, wl.splits, tf32)
+    check_close(outs, oracle_outputs(x, w_cat, wl.splits), mode_of(wl.dtype, tf32), name)
+
+
+EDGE = [
+    # (K, splits, M)
+    (72, (1, 3, 17), 1),          # K one box plus a ragged tail, tiny splits
+    (520, (33, 7), 3),            # K = 8 boxes + 8
+    (64, (1,), 1),                # one row, one box
+    (4096, (5000,), 2),           # more rows than one wave of CTAs
+    (5120, (1536, 576, 128, 64), 5),
+    (1024, (16, 16, 16, 16, 16, 16, 16, 16), 8),   # eight splits
+    (6144, (2048, 576, 128), 7),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("K,splits,M", EDGE)
+def test_edge_shapes(hsp, dtype, K, splits, M):
+    x, ws = W.random_case(K, splits, M, dtype, seed=K + M + len(splits))
+    w_cat = torch.cat(ws, 0)
+    for tf32 in ([False, True] if dtype == "fp32" else [False]):
+        outs = _run_both(hsp, x, w_cat, splits, tf32)
+        check_close(outs, oracle_outputs(x, w_cat, splits), mode_of(dtype, tf32), f"K{K}")
+
+
+@pytest.mark.parametrize("dtype,tf32", [("bf16", False), ("fp32", False), ("fp32", True)])
+def test_every_token_count(hsp, dtype, tf32):
+    K, splits = 1536, (200, 56)
+    for M in range(1, 65):
+        x, ws = W.random_case(K, splits, M, dtype, seed=500 + M)
+        w_cat = torch.cat(ws, 0)
+        outs = _run_both(hsp, x, w_cat, splits, tf32)
+        check_close(outs, oracle_outputs(x, w_cat, splits), mode_of(dtype, tf32), f"M{M}")
+
+
+@pytest.mark.parametrize("dtype,tf32", [("bf16", False), ("fp32", False), ("fp32", True)])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 33, 64])
+def test_small_integers_bit_exact(hsp, dtype, tf32, M):
+    # Every partial sum is an integer below 2^11: exact in fp32 and tf32 products,
+    # results within bf16's exact integer range.
+    K, splits = 64, (3, 16, 17)
+    x, ws = W.small_int_case(K, splits, M, dtype, seed=77 + M)
+    w_cat = torch.cat(ws, 0)
+    outs = _run_both(hsp, x, w_cat, splits, tf32)
+    ref = oracle_outputs(x, w_cat, splits)
+    for g, r in zip(outs, ref):
+        assert np.array_equal(as_f64(g), r)
+
+
+@pytest.mark.parametrize("dtype,tf32", [("bf16", False), ("fp32", False)])
+def test_one_hot_reproduces_columns(hsp, dtype, tf32):
+    K, splits = 5120, (1280, 512)
+    _, ws = W.random_case(K, splits, 1, dtype, seed=99)
+    w_cat = torch.cat(ws, 0)
+    cols = [0, 1, 63, 64, 511, 512, 2047, 4095, K - 2, K - 1]
+    x = torch.zeros(len(cols), K, dtype=w_cat.dtype)
+    for m, c in enumerate(cols):
+        x[m, c] = 1
+    outs = _run_both(hsp, x, w_cat, splits, tf32)
+    for wi, oi in zip(ws, outs):
+        for m, c in enumerate(cols):
+            assert torch.equal(oi[m].cpu(), wi[:, c]), (dtype, c)
+
+
+def test_zero_weights_and_negation(hsp):
+    K, splits = 7168, (1536, 576)
+    x, ws = W.random_case(K, splits, 8, "bf16", seed=5)
+    w_cat = torch.cat(ws, 0)
+    z = _run_both(hsp, x, torch.zeros_like(w_cat), splits)
+    assert all(torch.count_nonzero(o) == 0 for o in z)
+    pos = _run_both(hsp, x, w_cat, splits)
+    neg = _run_both(hsp, -x, w_cat, splits)
+    for p, n in zip(pos, neg):
+        assert torch.equal(p, -n)
+
+
+def test_empty_batch_is_a_no_op(hsp):
+    K, splits = 512, (16, 8)
+    w = torch.randn(24, K, device="cuda").to(torch.bfloat16)
+    x = torch.empty(0, K, device="cuda", dtype=torch.bfloat16)
+    before = hsp.launch_count()
+    outs = hsp.fused_gemm(x, w, splits)
+    assert [tuple(o.shape) for o in outs] == [(0, 16), (0, 8)]
+    assert hsp.launch_count() == before
