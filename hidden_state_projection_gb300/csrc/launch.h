@@ -1,7 +1,6 @@
 // launch.h -- host-side launch request for the streaming kernels.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "stream_args.h"
@@ -17,8 +16,6 @@ struct LaunchReq {
     int smem_bytes;  // dynamic shared memory
     int pdl;         // programmatic stream serialization
     cudaStream_t stream;
-    CUtensorMap tmap_w;
-    CUtensorMap tmap_x;
     StreamArgs args;
 };
 

@@ -46,7 +46,7 @@ cudaError_t launch_variant(const LaunchReq &r) {
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kern, r.tmap_w, r.tmap_x, r.args);
+    return cudaLaunchKernelEx(&cfg, kern, r.args);
 }
 
 template <int COMPUTE>

@@ -1,5 +1,5 @@
 // proj_api.cu -- the C ABI (include/proj.h): validation, the M-bucketed planner,
-// tensor-map encoding, the weight packer and the launch wrapper.
+// the weight packer and the launch wrapper.
 //
 // Dispatch (TensorRT-LLM PR #20636, Description: one fused call at one token,
 // one call per projection at 2-8 tokens, a different GEMM above): here every M in
@@ -12,9 +12,7 @@
 // bucket) only, so an output row is summed in the same order whatever the
 // number of rows in the launch -- the property that makes the fused and the
 // separate calls bitwise equal.
-#include <cuda.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cstdarg>
@@ -32,7 +30,7 @@ using hsp::LaunchReq;
 using hsp::StreamArgs;
 
 constexpr int kSmemLimit = 232448;          // per-block dynamic shared memory on sm_103
-constexpr int kSmemReserve = 1024 + 512;    // ring alignment slack + barriers + flags
+constexpr int kSmemReserve = 128 + 512;     // ring alignment slack + barriers + flags
 constexpr int kMaxRingStages = 32;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
@@ -112,72 +110,13 @@ proj_status device_info(DeviceInfo *out) {
     return PROJ_OK;
 }
 
-// ---- tensor maps -----------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-struct MapEntry {
-    uint64_t ptr, d0, d1, box1;
-    int dtype;
-    bool used;
-    CUtensorMap map;
-};
-constexpr int kMapCache = 128;
-std::mutex g_map_mu;
-MapEntry g_maps[kMapCache];
-int g_map_next = 0;
-
-proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0, uint32_t box1,
-                       proj_dtype dt, CUtensorMap *out) {
-    std::call_once(g_encode_once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    if (!g_encode) return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const uint64_t key = reinterpret_cast<uint64_t>(ptr);
-    {
-        std::lock_guard<std::mutex> lk(g_map_mu);
-        for (int i = 0; i < kMapCache; ++i) {
-            const MapEntry &m = g_maps[i];
-            if (m.used && m.ptr == key && m.d0 == d0 && m.d1 == d1 && m.box1 == box1 && m.dtype == dt) {
-                *out = m.map;
-                return PROJ_OK;
-            }
-        }
-    }
-    CUtensorMap map;
-    cuuint64_t dims[2] = {d0, d1};
-    cuuint64_t strides[1] = {d0 * static_cast<uint64_t>(elem_size(dt))};
-    cuuint32_t box[2] = {box0, box1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(&map, dt == PROJ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                          2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu], box [%u x %u]",
-                    static_cast<int>(r), (unsigned long long)d1, (unsigned long long)d0, box1, box0);
-    {
-        std::lock_guard<std::mutex> lk(g_map_mu);
-        MapEntry &m = g_maps[g_map_next];
-        g_map_next = (g_map_next + 1) % kMapCache;
-        m = MapEntry{key, d0, d1, box1, static_cast<int>(dt), true, map};
-    }
-    *out = map;
-    return PROJ_OK;
-}
-
 // ---- planner -----------------------------------------------------------------
 
 struct Plan {
     proj_plan_info info;
     int compute, bucket, MT, RT, WR, WK, S, R, grid_x;
-    int kboxes, T, Ts, ring_stages, stage_bytes, w_box_bytes, x_box_bytes, ring_bytes, smem;
+    int units_total, units_per_slice, stage_units, stages_per_slice, ring_stages;
+    int pitch, stage_bytes, ring_bytes, smem;
 };
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -194,49 +133,70 @@ proj_status check_shape(int32_t M, int32_t K, int64_t n_total, int dt) {
     return PROJ_OK;
 }
 
+// Geometry of one launch over n_rows weight rows.
+//   - bucket, WK, S and units_per_slice depend on (M's bucket, K, dtype) only:
+//     they fix which warp and which K slice sums every 128-byte unit of K, hence
+//     the summation order of every output;
+//   - R (rows per CTA) spreads the rows over the SMs and the stage width is the
+//     widest that still leaves two ring stages in shared memory: long contiguous
+//     row segments per bulk copy.  Neither changes the order.
 void make_plan(int M, int K, int n_rows, proj_dtype dt, int sms, Plan *p) {
     memset(p, 0, sizeof *p);
     const int esz = elem_size(dt);
-    const int boxk = 128 / esz;
     p->compute = dt == PROJ_BF16 ? hsp::kMmaBf16 : (dt == PROJ_TF32 ? hsp::kMmaTf32 : hsp::kFmaFp32);
     p->bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
     static const int WRs[3] = {1, 2, 4}, WKs[3] = {8, 4, 2};
     p->WR = WRs[p->bucket];
     p->WK = WKs[p->bucket];
     p->MT = p->bucket == 0 ? 1 : (p->bucket == 2 ? 8 : (M <= 16 ? 2 : 4));
-    p->kboxes = ceil_div(K, boxk);
-    p->T = ceil_div(p->kboxes, p->WK);
-    // K slices: a function of (K, dtype, bucket) only (never of the row count).
+    const int64_t row_bytes = static_cast<int64_t>(K) * esz;
+    p->units_total = static_cast<int>((row_bytes + hsp::kUnitBytes - 1) / hsp::kUnitBytes);
+    // K slices (clusters) only for the larger token buckets, where one CTA's
+    // token rows of X would not fit next to a useful weight stage otherwise.
+    const int per_warp = ceil_div(p->units_total, p->WK);
     p->S = 1;
     if (p->bucket > 0) {
-        if (p->T >= 16) p->S = 4;
-        else if (p->T >= 4) p->S = 2;
+        if (per_warp >= 16) p->S = 4;
+        else if (per_warp >= 4) p->S = 2;
     }
-    p->Ts = ceil_div(p->T, p->S);
+    p->units_per_slice = ceil_div(ceil_div(p->units_total, p->S), p->WK) * p->WK;
+    while (p->S > 1 && (p->S - 1) * p->units_per_slice >= p->units_total) {  // no empty slice
+        --p->S;
+        p->units_per_slice = ceil_div(ceil_div(p->units_total, p->S), p->WK) * p->WK;
+    }
     const int max_rows = p->WR * 2 * 16;
-    if (p->bucket == 0) {
-        p->R = ceil_div(n_rows, sms);
-    } else {
-        p->R = ceil_div(n_rows * p->S, sms);
-    }
+    p->R = p->bucket == 0 ? ceil_div(n_rows, sms) : ceil_div(n_rows * p->S, sms);
     if (p->R < 1) p->R = 1;
     if (p->R > max_rows) p->R = max_rows;
-    p->RT = ceil_div(p->R, p->WR * 16) > 1 ? 2 : 1;
+    p->RT = p->R > p->WR * 16 ? 2 : 1;
     const int slots = p->WR * p->RT * 16;
     p->grid_x = ceil_div(n_rows, p->R);
-    p->w_box_bytes = slots * 128;
-    p->x_box_bytes = 8 * p->MT * 128;
-    p->stage_bytes = p->WK * (p->w_box_bytes + p->x_box_bytes);
-    const int budget = kSmemLimit - kSmemReserve;
-    int stages = budget / p->stage_bytes;
-    if (stages > p->Ts) stages = p->Ts;
-    if (stages > kMaxRingStages) stages = kMaxRingStages;
-    if (stages < 1) stages = 1;
-    p->ring_stages = stages;
     const int red_bytes = p->WK * slots * 8 * p->MT * 4;
-    p->ring_bytes = stages * p->stage_bytes;
+    const int budget = kSmemLimit - kSmemReserve;
+    const int Us = p->units_per_slice;
+    const int first = Us >= 2 * p->WK ? 2 : 1;
+    for (int nst = first; nst <= Us; ++nst) {
+        int su = ceil_div(Us, nst);
+        if (su > p->WK) su = ceil_div(su, p->WK) * p->WK;
+        const int n_eff = ceil_div(Us, su);
+        const int pitch = su * hsp::kUnitBytes + 16;
+        const int stage = (p->R + M) * pitch;
+        int ring = budget / stage;
+        if (ring > n_eff) ring = n_eff;
+        if (ring > kMaxRingStages) ring = kMaxRingStages;
+        if (ring >= (n_eff >= 2 ? 2 : 1) && ring * stage >= 0) {
+            p->stage_units = su;
+            p->stages_per_slice = n_eff;
+            p->ring_stages = ring;
+            p->pitch = pitch;
+            p->stage_bytes = stage;
+            break;
+        }
+    }
+    p->ring_bytes = p->ring_stages * p->stage_bytes;
     if (p->ring_bytes < red_bytes) p->ring_bytes = red_bytes;
-    p->smem = 1024 + p->ring_bytes + 2 * stages * 8 + 8 + 4 * stages + 64;
+    p->ring_bytes = ceil_div(p->ring_bytes, 128) * 128;
+    p->smem = 128 + p->ring_bytes + 2 * p->ring_stages * 8 + 8 + 4 * p->ring_stages + 64;
     proj_plan_info &i = p->info;
     i.bucket = p->bucket;
     i.compute = p->compute;
@@ -250,25 +210,20 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, int sms, Plan *p) {
     i.ring_stages = p->ring_stages;
     i.stage_bytes = p->stage_bytes;
     i.smem_bytes = p->smem;
-    i.k_per_stage = p->WK * boxk;
-    i.stages_total = p->T;
+    i.k_per_stage = p->stage_units * hsp::kUnitBytes / esz;
+    i.stages_total = p->stages_per_slice;
     i.threads = hsp::kThreadsPerCta;
+    i.units_per_slice = p->units_per_slice;
 }
 
-// One launch over `n_rows` rows of a weight map starting at `w` (already offset).
+// One launch over `n_rows` weight rows starting at `w` (already offset to the first row).
 proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
                         proj_dtype dt, const hsp::SplitTable &splits, cudaStream_t stream) {
     Plan p;
     make_plan(M, K, n_rows, dt, dev.sms, &p);
-    if (p.smem > kSmemLimit) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "plan needs %d bytes of shared memory", p.smem);
-    const uint32_t boxk = 128 / elem_size(dt);
+    if (p.ring_stages < 1 || p.smem > kSmemLimit)
+        return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "no shared-memory plan for M=%d K=%d rows=%d", M, K, n_rows);
     LaunchReq r{};
-    proj_status st = encode_map(w, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), boxk,
-                                static_cast<uint32_t>(p.R), dt, &r.tmap_w);
-    if (st != PROJ_OK) return st;
-    st = encode_map(x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), boxk, static_cast<uint32_t>(8 * p.MT), dt,
-                    &r.tmap_x);
-    if (st != PROJ_OK) return st;
     r.compute = p.compute;
     r.bucket = p.bucket;
     r.MT = p.MT;
@@ -278,19 +233,20 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
     r.pdl = g_opt_pdl.load();
     r.stream = stream;
     StreamArgs &a = r.args;
+    a.w = static_cast<const char *>(w);
+    a.x = static_cast<const char *>(x);
+    a.row_bytes = static_cast<int64_t>(K) * elem_size(dt);
     a.n_rows = n_rows;
     a.rows_per_cta = p.R;
     a.M = M;
-    a.kboxes = p.kboxes;
-    a.stages_total = p.T;
-    a.stages_per_slice = p.Ts;
+    a.units_total = p.units_total;
+    a.units_per_slice = p.units_per_slice;
+    a.stage_units = p.stage_units;
+    a.stages_per_slice = p.stages_per_slice;
     a.ring_stages = p.ring_stages;
     a.slices = p.S;
+    a.pitch = static_cast<uint32_t>(p.pitch);
     a.stage_bytes = static_cast<uint32_t>(p.stage_bytes);
-    a.w_box_bytes = static_cast<uint32_t>(p.w_box_bytes);
-    a.x_box_bytes = static_cast<uint32_t>(p.x_box_bytes);
-    a.w_tx_bytes = static_cast<uint32_t>(p.R * 128);
-    a.x_tx_bytes = static_cast<uint32_t>(8 * p.MT * 128);
     a.ring_bytes = static_cast<uint32_t>(p.ring_bytes);
     a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
     const int wus = g_opt_wait_us.load();

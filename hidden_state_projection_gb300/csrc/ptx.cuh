@@ -1,8 +1,9 @@
 // ptx.cuh -- thin inline-PTX wrappers used by the streaming kernels (sm_103a).
 //
 // Only instructions documented in the PTX ISA are used: mbarrier phase
-// tracking, TMA tensor copies into shared memory, ldmatrix, mma.sync,
-// griddepcontrol (programmatic dependent launch) and cluster shared memory.
+// tracking, bulk (TMA-engine) copies into shared memory with L2 cache hints,
+// ldmatrix, mma.sync, griddepcontrol (programmatic dependent launch) and
+// cluster shared memory.
 #pragma once
 
 #include <cuda.h>
@@ -60,22 +61,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// ---- TMA ------------------------------------------------------------------
+// ---- bulk copies (TMA engine, untiled) --------------------------------------
 
-__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+// L2 policy for data read exactly once (the weights): evict first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
-// 2-D tiled copy global -> shared, completion counted on `bar` in bytes.
-// c0 is the innermost (contiguous) coordinate; it is always a multiple of the
-// 128-byte box width here, so the 16-byte start rule holds.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0,
-                                            int32_t c1, uint32_t bar) {
+// Contiguous global -> shared copy of `bytes` (multiple of 16; both addresses
+// 16-byte aligned), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Order this thread's generic-proxy shared-memory writes before later async-proxy
+// (bulk copy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---- shared-memory fragments and tensor-core products ---------------------

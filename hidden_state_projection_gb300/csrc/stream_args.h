@@ -9,8 +9,9 @@ enum Compute : int { kMmaBf16 = 0, kMmaTf32 = 1, kFmaFp32 = 2 };
 
 constexpr int kMaxSplits = 8;
 constexpr int kDeviceErrTimeout = 7;  // same value as PROJ_ERR_TIMEOUT
+constexpr int kUnitBytes = 128;       // one k-unit: 128 bytes of a row (64 bf16 or 32 fp32)
 
-// Output scatter: row n of the launch (0-based in its weight map) belongs to
+// Output scatter: row n of the launch (0-based in its weight rows) belongs to
 // split i with off[i] <= n < off[i] + rows[i]; element (token t, row n) goes to
 // out[i][t * rows[i] + (n - off[i])].
 struct SplitTable {
@@ -20,22 +21,28 @@ struct SplitTable {
     void *out[kMaxSplits];
 };
 
+// K is cut into units of 128 bytes.  Unit u is summed by warp (u mod WK) of the
+// CTA that owns its K slice (slice s holds units [s*units_per_slice, ...)); a
+// ring stage carries stage_units consecutive units of every row of the CTA and
+// of every token.  Only the unit -> warp -> slice map decides the summation
+// order; the stage width and the row count do not.
 struct StreamArgs {
-    int32_t n_rows;            // rows of the launch's weight map
-    int32_t rows_per_cta;      // R (the W box height)
+    const char *w;             // first weight row of the launch, [n_rows, K] row-major
+    const char *x;             // activations, [M, K] row-major
+    int64_t row_bytes;         // K * element size (a multiple of 16)
+    int32_t n_rows;            // rows of the launch
+    int32_t rows_per_cta;      // R
     int32_t M;                 // tokens
-    int32_t kboxes;            // ceil(K / box width)
-    int32_t stages_total;      // ceil(kboxes / WK)
-    int32_t stages_per_slice;  // stages owned by one K slice
+    int32_t units_total;       // ceil(row_bytes / 128)
+    int32_t units_per_slice;   // units of one K slice
+    int32_t stage_units;       // units per ring stage
+    int32_t stages_per_slice;  // ceil(units_per_slice / stage_units)
     int32_t ring_stages;       // shared-memory ring depth
     int32_t slices;            // S (cluster size along grid.y)
-    uint32_t stage_bytes;      // WK * (w_box_bytes + x_box_bytes)
-    uint32_t w_box_bytes;      // shared footprint of one W box (row slots * 128)
-    uint32_t x_box_bytes;      // 8 * MT * 128
-    uint32_t w_tx_bytes;       // bytes one W box delivers (R * 128)
-    uint32_t x_tx_bytes;       // bytes one X box delivers (8 * MT * 128)
+    uint32_t pitch;            // shared-memory row pitch of a stage (stage_units*128 + 16)
+    uint32_t stage_bytes;      // (R + M) * pitch
     uint32_t ring_bytes;       // ring_stages * stage_bytes, at least the reduction buffer
-    int32_t skip_stage;        // test hook: this global stage is never loaded (-1: off)
+    int32_t skip_stage;        // test hook: this stage of every slice is never loaded (-1: off)
     int32_t pad_;
     uint64_t wait_limit_ns;    // bound of every barrier wait
     int *err_word;             // device error word (PROJ_ERR_TIMEOUT on expiry)

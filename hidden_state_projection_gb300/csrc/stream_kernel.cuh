@@ -1,22 +1,27 @@
 // stream_kernel.cuh -- the weight-streaming projection kernel.
 //
-// Computes, for the rows [row0, row0 + R) of one launch's weight map and all M
+// Computes, for the rows [row0, row0 + R) of one launch's weight rows and all M
 // tokens,  y[m][n] = sum_k x[m][k] * w[n][k]  with fp32 accumulation, rounds once
 // and scatters every row into the output of the projection it belongs to
 // (TensorRT-LLM PR #20636, Description: one GEMM over the row-concatenated
 // weight, halves returned as dense [M, N_i] outputs).
 //
-// Structure of one CTA (the design of the pages' GLM fused-A kernel -- weights
-// staged by tensor copies before the grid-dependency wait, activations after
-// it, warp sums added in warp order and rounded once; TensorRT-LLM PR #20502,
-// glmFusedAGemm commit message -- re-drawn for TMA rings and clusters):
+// Structure of one CTA (after the pages' GLM fused-A kernel -- weights copied
+// in before the grid-dependency wait, activations after it, warp sums added in
+// warp order and rounded once; TensorRT-LLM PR #20502, glmFusedAGemm commit
+// message -- re-drawn for bulk-copy rings and clusters on sm_103a):
 //
-//   * warp kNCW (the producer) issues 2-D TMA copies of 128-byte-wide boxes of
-//     W (R rows) and X (8*MT token rows) into a ring of shared-memory stages;
-//     the W boxes of the first ring's worth of stages go out before
-//     griddepcontrol.wait, the X boxes only after it;
-//   * consumer warp (wr, wk) takes box wk of every stage, for its RT 16-row
-//     tiles, and accumulates in registers: mma.sync bf16 / tf32, or fp32 FMA;
+//   * warp kNCW (the producer) fills a ring of shared-memory stages with 1-D bulk
+//     copies: one copy per weight row and per token row, each a contiguous
+//     segment of stage_units * 128 bytes (long contiguous reads keep DRAM pages
+//     open; 128-byte pieces at the row pitch do not).  The weight copies of the
+//     first ring's worth of stages are issued before griddepcontrol.wait, the
+//     activation copies only after it;
+//   * shared rows are padded to a pitch of 16 mod 128 bytes, so the eight rows
+//     an ldmatrix phase reads fall in eight different bank groups;
+//   * consumer warp (wr, wk) takes every k-unit u (128 bytes of K) of a stage
+//     with u mod WK == wk, for its RT 16-row tiles, and accumulates in registers
+//     (mma.sync bf16 / tf32, or fp32 FMA);
 //   * the WK warp partials of each output are added in warp order, then (S > 1)
 //     the S CTAs of a cluster, each holding one K slice, add their partials in
 //     slice order through distributed shared memory;
@@ -26,9 +31,13 @@
 //     recommends).
 //
 // Determinism: the summation order of an output depends only on (K, the element
-// type, WK, S) -- never on the row count, the row's position in a tile, the grid
-// or the arrival order -- so fused and per-projection launches, repeated runs
-// and graph replays give identical bits.
+// type, WK, S) -- never on the row count, the stage width, the row's position in a
+// tile, the grid or the arrival order -- so fused and per-projection launches,
+// repeated runs and graph replays give identical bits.
+//
+// Rows past the CTA's last weight row, and token rows past M, are never loaded:
+// their fragment reads are clamped to the last loaded row, and their results are
+// never stored.  A final partial k-unit is zero-filled in shared memory before use.
 //
 // Every wait on a shared-memory barrier is bounded (globaltimer); on expiry the
 // kernel records PROJ_ERR_TIMEOUT in the device error word, stops computing,
@@ -36,7 +45,6 @@
 // returns through the same barriers as a normal exit.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -51,18 +59,10 @@ struct StreamCfg {
     static constexpr int kNCW = WR * WK;                 // consumer warps
     static constexpr int kThreads = (kNCW + 1) * 32;     // + producer warp
     static constexpr int kSlots = WR * RT * 16;          // row slots per CTA
-    static constexpr int kXRows = 8 * MT;                // token rows per X box
-    static constexpr int kEsz = (COMPUTE == kMmaBf16) ? 2 : 4;
-    static constexpr int kBoxK = 128 / kEsz;             // K elements per box
+    static constexpr int kXRows = 8 * MT;                // token slots
     static_assert(WR * WK == 8, "eight consumer warps");
     static_assert(MT == 1 || MT % 2 == 0, "token tiles: 1 or even");
 };
-
-// Byte offset of 16-byte chunk c of row r inside a box written by TMA with
-// 128-byte swizzling (box base 1024-byte aligned): chunk index XOR (row mod 8).
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return static_cast<uint32_t>(r * 128 + (((c ^ r) & 7) << 4));
-}
 
 // Warp-wide bounded wait on one barrier phase.  True when the phase completed;
 // false when the limit ran out or another warp already gave up.
@@ -94,24 +94,33 @@ __device__ __forceinline__ void record_timeout(int *err_word, volatile int *abor
     *abort_flag = 1;
 }
 
-// ---- inner products on one staged box ------------------------------------
+// Shared-memory view of one stage: weight rows [0, R) then token rows [0, M),
+// each `pitch` bytes apart; reads past the loaded rows are clamped.
+struct StageView {
+    uint32_t w, x;     // shared addresses of weight row 0 / token row 0
+    uint32_t pitch;
+    int rmax, tmax;    // last loaded weight row / token row
+    __device__ __forceinline__ uint32_t wrow(int r) const { return w + static_cast<uint32_t>(min(r, rmax)) * pitch; }
+    __device__ __forceinline__ uint32_t xrow(int t) const { return x + static_cast<uint32_t>(min(t, tmax)) * pitch; }
+};
 
-// Tensor-core box: 4 k-steps (k16 for bf16, k8 for tf32) over the warp's row tiles.
+// ---- inner products on one 128-byte k-unit at byte offset `ub` of the stage ----
+
+// Tensor cores: 4 k-steps (k16 for bf16, k8 for tf32) over the warp's row tiles.
 template <class C, int RT, int MT>
-__device__ __forceinline__ void box_mma(uint32_t wbox, uint32_t xbox, int wr, int lane,
-                                        float (&acc)[RT][MT][4]) {
+__device__ __forceinline__ void unit_mma(const StageView &v, uint32_t ub, int wr, int lane,
+                                         float (&acc)[RT][MT][4]) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
         uint32_t b[MT][2];
+        const uint32_t bb = ub + ks * 32 + ((lane >> 3) & 1) * 16;
         if constexpr (MT == 1) {
-            const int tok = lane & 7, c = 2 * ks + ((lane >> 3) & 1);
-            ldsm_x2(xbox + swz(tok, c), b[0][0], b[0][1]);
+            ldsm_x2(v.xrow(lane & 7) + bb, b[0][0], b[0][1]);
         } else {
 #pragma unroll
             for (int j = 0; j < MT; j += 2) {
                 const int tok = (j + (lane >> 4)) * 8 + (lane & 7);
-                const int c = 2 * ks + ((lane >> 3) & 1);
-                ldsm_x4(xbox + swz(tok, c), b[j][0], b[j][1], b[j + 1][0], b[j + 1][1]);
+                ldsm_x4(v.xrow(tok) + bb, b[j][0], b[j][1], b[j + 1][0], b[j + 1][1]);
             }
         }
         if constexpr (C::kCompute == kMmaTf32) {
@@ -121,12 +130,11 @@ __device__ __forceinline__ void box_mma(uint32_t wbox, uint32_t xbox, int wr, in
                 b[j][1] = to_tf32(b[j][1]);
             }
         }
+        const uint32_t ab = ub + ks * 32 + (lane >> 4) * 16;
 #pragma unroll
         for (int t = 0; t < RT; ++t) {
-            const int r = wr * RT * 16 + t * 16 + (lane & 15);
-            const int c = 2 * ks + (lane >> 4);
             uint32_t a[4];
-            ldsm_x4(wbox + swz(r, c), a[0], a[1], a[2], a[3]);
+            ldsm_x4(v.wrow(wr * RT * 16 + t * 16 + (lane & 15)) + ab, a[0], a[1], a[2], a[3]);
             if constexpr (C::kCompute == kMmaTf32) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) a[q] = to_tf32(a[q]);
@@ -140,20 +148,21 @@ __device__ __forceinline__ void box_mma(uint32_t wbox, uint32_t xbox, int wr, in
     }
 }
 
-// FP32 FMA box, few tokens (MT == 1): lane = (row group g = lane/8, chunk c = lane%8).
-// Each lane owns rows wr*RT*16 + g + 4i (i < 4RT) for all 8 token rows and the
+// FP32 FMA, few tokens (MT == 1): lane = (row group g = lane/8, 16-byte chunk c = lane%8).
+// Each lane owns rows wr*RT*16 + g + 4i (i < 4RT) for the 8 token slots and the
 // 4 consecutive k of chunk c; the 8 chunk lanes are added by a fixed butterfly
 // at the end.  acc[i][t]: row i, token t.
 template <class C, int RT>
-__device__ __forceinline__ void box_fma_ksplit(uint32_t wbox, uint32_t xbox, int wr, int lane,
-                                               int M, float (&acc)[4 * RT][8]) {
+__device__ __forceinline__ void unit_fma_ksplit(const StageView &v, uint32_t ub, int wr, int lane, int M,
+                                                float (&acc)[4 * RT][8]) {
     const int c = lane & 7, g = lane >> 3;
+    const uint32_t cb = ub + c * 16;
     float4 xv[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) xv[t] = lds128(xbox + swz(t, c));
+    for (int t = 0; t < 8; ++t) xv[t] = lds128(v.xrow(t) + cb);
 #pragma unroll
     for (int i = 0; i < 4 * RT; ++i) {
-        const float4 wv = lds128(wbox + swz(wr * RT * 16 + g + 4 * i, c));
+        const float4 wv = lds128(v.wrow(wr * RT * 16 + g + 4 * i) + cb);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             if (t < M) {
@@ -166,20 +175,20 @@ __device__ __forceinline__ void box_fma_ksplit(uint32_t wbox, uint32_t xbox, int
     }
 }
 
-// FP32 FMA box, many tokens (MT >= 2): lane = (row lane rl = lane%4, token lane
+// FP32 FMA, many tokens (MT >= 2): lane = (row lane rl = lane%4, token lane
 // tl = lane/4); rows wr*RT*16 + rl + 4i (i < 4RT), tokens tl + 8j (j < MT); each
 // output is one sequential fma chain over k.
 template <class C, int RT, int MT>
-__device__ __forceinline__ void box_fma_outer(uint32_t wbox, uint32_t xbox, int wr, int lane,
-                                              float (&acc)[4 * RT][MT]) {
+__device__ __forceinline__ void unit_fma_outer(const StageView &v, uint32_t ub, int wr, int lane,
+                                               float (&acc)[4 * RT][MT]) {
     const int rl = lane & 3, tl = lane >> 2;
 #pragma unroll 2
     for (int c = 0; c < 8; ++c) {
         float4 wv[4 * RT], xv[MT];
 #pragma unroll
-        for (int i = 0; i < 4 * RT; ++i) wv[i] = lds128(wbox + swz(wr * RT * 16 + rl + 4 * i, c));
+        for (int i = 0; i < 4 * RT; ++i) wv[i] = lds128(v.wrow(wr * RT * 16 + rl + 4 * i) + ub + c * 16);
 #pragma unroll
-        for (int j = 0; j < MT; ++j) xv[j] = lds128(xbox + swz(tl + 8 * j, c));
+        for (int j = 0; j < MT; ++j) xv[j] = lds128(v.xrow(tl + 8 * j) + ub + c * 16);
 #pragma unroll
         for (int i = 0; i < 4 * RT; ++i)
 #pragma unroll
@@ -190,6 +199,19 @@ __device__ __forceinline__ void box_fma_outer(uint32_t wbox, uint32_t xbox, int 
                 acc[i][j] = fmaf(wv[i].w, xv[j].w, acc[i][j]);
             }
     }
+}
+
+// Zero the bytes [valid, 128) of one k-unit in every loaded row (the tail of K).
+__device__ __forceinline__ void zero_unit_tail(const StageView &v, uint32_t ub, uint32_t valid, int lane) {
+    const int chunks = static_cast<int>((128u - valid) >> 4);
+    const int rows = v.rmax + 1 + v.tmax + 1;
+    for (int idx = lane; idx < rows * chunks; idx += 32) {
+        const int r = idx / chunks, c = idx - r * chunks;
+        const uint32_t base = (r <= v.rmax) ? v.wrow(r) : v.xrow(r - v.rmax - 1);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + ub + valid + c * 16), "r"(0u)
+                     : "memory");
+    }
+    __syncwarp();
 }
 
 // ---- output scatter -------------------------------------------------------
@@ -211,15 +233,13 @@ __device__ __forceinline__ void store_out(const StreamArgs &a, int n, int tok, f
 
 template <int COMPUTE, int MT, int RT, int WR, int WK>
 __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 1)
-    hsp_stream_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                      const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ StreamArgs a) {
+    hsp_stream_kernel(const __grid_constant__ StreamArgs a) {
     using C = StreamCfg<COMPUTE, MT, RT, WR, WK>;
-    constexpr int kSlots = C::kSlots, kXRows = C::kXRows, kBoxK = C::kBoxK;
+    constexpr int kSlots = C::kSlots, kXRows = C::kXRows;
 
-    extern __shared__ uint8_t smem_raw[];
-    // Align the ring to 1024 bytes in the shared window (swizzle atom).
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *smem = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
     const uint32_t ring = smem_u32(smem);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.ring_bytes);
     uint64_t *empty = full + a.ring_stages;
@@ -228,9 +248,11 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row0 = blockIdx.x * a.rows_per_cta;
-    const int g0 = blockIdx.y * a.stages_per_slice;
-    const int nst = max(0, min(a.stages_total, g0 + a.stages_per_slice) - g0);
-    const uint32_t x_region = WK * a.w_box_bytes;  // X boxes follow the W boxes in a stage
+    const int rows_here = min(a.rows_per_cta, a.n_rows - row0);
+    const int slice = blockIdx.y;
+    const int u_slice0 = slice * a.units_per_slice;
+    const int u_slice1 = min(a.units_total, u_slice0 + a.units_per_slice);
+    const int nst = max(0, (u_slice1 - u_slice0 + a.stage_units - 1) / a.stage_units);
 
     if (tid == 0) {
         for (int s = 0; s < a.ring_stages; ++s) {
@@ -256,31 +278,45 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     if (warp == C::kNCW) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            tma_prefetch_map(&tmap_w);
-            tma_prefetch_map(&tmap_x);
+            const uint64_t w_policy = l2_policy_evict_first();
+            const char *wrow0 = a.w + static_cast<int64_t>(row0) * a.row_bytes;
+            auto span = [&](int i, int64_t &byte0, uint32_t &nbytes) {
+                const int u0 = u_slice0 + i * a.stage_units;
+                const int u1 = min(u0 + a.stage_units, u_slice1);
+                byte0 = static_cast<int64_t>(u0) * kUnitBytes;
+                const int64_t end = min(static_cast<int64_t>(u1) * kUnitBytes, a.row_bytes);
+                nbytes = static_cast<uint32_t>(end - byte0);
+            };
+            auto issue_w = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
+                const uint32_t base = ring + slot * a.stage_bytes;
+                for (int r = 0; r < rows_here; ++r)
+                    bulk_load_hint(base + r * a.pitch, wrow0 + r * a.row_bytes + byte0, nbytes, fb, w_policy);
+            };
+            auto issue_x = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
+                const uint32_t base = ring + slot * a.stage_bytes + a.rows_per_cta * a.pitch;
+                for (int t = 0; t < a.M; ++t) bulk_load(base + t * a.pitch, a.x + t * a.row_bytes + byte0, nbytes, fb);
+            };
             const int npre = min(nst, a.ring_stages);
             // Weights of the first ring's worth of stages: before the grid dependency.
             for (int i = 0; i < npre; ++i) {
-                const int g = g0 + i;
-                if (g == a.skip_stage) continue;
-                const int nb = min(WK, a.kboxes - g * WK);
+                if (i == a.skip_stage) continue;
+                int64_t b0;
+                uint32_t nb;
+                span(i, b0, nb);
                 const uint32_t fb = smem_u32(&full[i]);
-                const uint32_t base = ring + i * a.stage_bytes;
-                mbar_expect_tx(fb, nb * a.w_tx_bytes);
-                for (int j = 0; j < nb; ++j)
-                    tma_load_2d(base + j * a.w_box_bytes, &tmap_w, (g * WK + j) * kBoxK, row0, fb);
+                mbar_expect_tx(fb, static_cast<uint32_t>(rows_here) * nb);
+                issue_w(i, b0, nb, fb);
             }
             // Activations are written by the previous kernel on the stream.
             griddep_wait();
             for (int i = 0; i < npre; ++i) {
-                const int g = g0 + i;
-                if (g == a.skip_stage) continue;
-                const int nb = min(WK, a.kboxes - g * WK);
+                if (i == a.skip_stage) continue;
+                int64_t b0;
+                uint32_t nb;
+                span(i, b0, nb);
                 const uint32_t fb = smem_u32(&full[i]);
-                const uint32_t base = ring + i * a.stage_bytes + x_region;
-                mbar_arrive_expect_tx(fb, nb * a.x_tx_bytes);
-                for (int j = 0; j < nb; ++j)
-                    tma_load_2d(base + j * a.x_box_bytes, &tmap_x, (g * WK + j) * kBoxK, 0, fb);
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.M) * nb);
+                issue_x(i, b0, nb, fb);
                 armed[i] = i;
             }
             for (int i = npre; i < nst; ++i) {
@@ -290,17 +326,14 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                     record_timeout(a.err_word, abort_flag);
                     break;
                 }
-                const int g = g0 + i;
-                if (g == a.skip_stage) continue;
-                const int nb = min(WK, a.kboxes - g * WK);
+                if (i == a.skip_stage) continue;
+                int64_t b0;
+                uint32_t nb;
+                span(i, b0, nb);
                 const uint32_t fb = smem_u32(&full[slot]);
-                const uint32_t base = ring + slot * a.stage_bytes;
-                mbar_arrive_expect_tx(fb, nb * (a.w_tx_bytes + a.x_tx_bytes));
-                for (int j = 0; j < nb; ++j)
-                    tma_load_2d(base + j * a.w_box_bytes, &tmap_w, (g * WK + j) * kBoxK, row0, fb);
-                for (int j = 0; j < nb; ++j)
-                    tma_load_2d(base + x_region + j * a.x_box_bytes, &tmap_x, (g * WK + j) * kBoxK,
-                                0, fb);
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows_here + a.M) * nb);
+                issue_w(slot, b0, nb, fb);
+                issue_x(slot, b0, nb, fb);
                 armed[slot] = i;
             }
         }
@@ -308,7 +341,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     } else {
         // ---------------- consumers ----------------
         const int wk = warp % WK, wr = warp / WK;
-        const bool has_rows = wr * RT * 16 < a.rows_per_cta;
+        const bool has_rows = wr * RT * 16 < rows_here;
         for (int i = 0; i < nst; ++i) {
             const int slot = i % a.ring_stages;
             const uint32_t par = static_cast<uint32_t>(i / a.ring_stages) & 1u;
@@ -316,25 +349,41 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 if (lane == 0) record_timeout(a.err_word, abort_flag);
                 break;
             }
-            const int b = (g0 + i) * WK + wk;
-            if (b < a.kboxes && has_rows) {
-                const uint32_t wbox = ring + slot * a.stage_bytes + wk * a.w_box_bytes;
-                const uint32_t xbox = ring + slot * a.stage_bytes + x_region + wk * a.x_box_bytes;
+            const int u0 = u_slice0 + i * a.stage_units;
+            const int u1 = min(u0 + a.stage_units, u_slice1);
+            StageView v;
+            v.w = ring + slot * a.stage_bytes;
+            v.x = v.w + a.rows_per_cta * a.pitch;
+            v.pitch = a.pitch;
+            v.rmax = rows_here - 1;
+            v.tmax = a.M - 1;
+            bool zeroed = false;
+            // units of this warp: u = u0 + j with u mod WK == wk, in increasing order
+            int u = u0 + ((wk - u0 % WK) % WK + WK) % WK;
+            for (; u < u1; u += WK) {
+                const uint32_t ub = static_cast<uint32_t>(u - u0) * kUnitBytes;
+                const int64_t valid = a.row_bytes - static_cast<int64_t>(u) * kUnitBytes;
+                if (valid < kUnitBytes) {
+                    zero_unit_tail(v, ub, static_cast<uint32_t>(valid), lane);
+                    zeroed = true;
+                }
+                if (!has_rows) continue;
                 if constexpr (COMPUTE == kFmaFp32) {
                     if constexpr (MT == 1)
-                        box_fma_ksplit<C, RT>(wbox, xbox, wr, lane, a.M, acc_fk);
+                        unit_fma_ksplit<C, RT>(v, ub, wr, lane, a.M, acc_fk);
                     else
-                        box_fma_outer<C, RT, MT>(wbox, xbox, wr, lane, acc_fo);
+                        unit_fma_outer<C, RT, MT>(v, ub, wr, lane, acc_fo);
                 } else {
-                    box_mma<C, RT, MT>(wbox, xbox, wr, lane, acc_mma);
+                    unit_mma<C, RT, MT>(v, ub, wr, lane, acc_mma);
                 }
             }
+            if (zeroed) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
         }
     }
 
-    // All ring reads are done (or abandoned).  [A]
+    // All ring reads are done (or abandoned).
     __syncthreads();
     const bool aborted = (*abort_flag != 0);
     if (aborted) {
@@ -400,7 +449,6 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     griddep_wait();
 
     // ---- warp partials added in warp order; single-slice CTAs store here ----
-    const int rows_here = min(a.rows_per_cta, a.n_rows - row0);
     if (!aborted) {
         for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
             const int tok = e / kSlots, slot = e - tok * kSlots;
@@ -420,10 +468,9 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         cluster_sync_all();
         if (!aborted) {
             const int per = kSlots / a.slices;
-            const int my = static_cast<int>(blockIdx.y);
             const uint32_t red_local = smem_u32(red);
             for (int e = tid; e < per * kXRows; e += C::kThreads) {
-                const int tok = e / per, slot = my * per + (e - tok * per);
+                const int tok = e / per, slot = slice * per + (e - tok * per);
                 if (tok >= a.M || slot >= rows_here) continue;
                 const uint32_t off = red_local + static_cast<uint32_t>((slot * kXRows + tok) * 4);
                 float v = ld_shared_cluster_f32(cluster_map_shared(off, 0));

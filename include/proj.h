@@ -100,9 +100,10 @@ typedef struct {
     int32_t stage_bytes;
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t k_per_stage;   /* elements of K per ring stage */
-    int32_t stages_total;  /* ring stages over all of K */
+    int32_t stages_total;  /* ring stages of one K slice */
     int32_t threads;       /* threads per CTA (consumer warps + 1 producer warp) */
-    int32_t reserved[5];
+    int32_t units_per_slice; /* 128-byte k-units per K slice (fixes the summation order with k_warps) */
+    int32_t reserved[4];
 } proj_plan_info;
 
 /*

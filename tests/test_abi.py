@@ -101,7 +101,7 @@ def test_k_split_independent_of_rows(hsp, name):
             full = hsp.describe_plan(M, wl.K, wl.n_total, dt)
             for n in list(wl.splits) + [1, 3, 17, 5000]:
                 part = hsp.describe_plan(M, wl.K, n, dt)
-                for key in ("bucket", "k_warps", "slices", "k_per_stage", "stages_total", "compute"):
+                for key in ("bucket", "k_warps", "slices", "units_per_slice", "compute"):
                     assert part[key] == full[key], (name, M, n, key)
 
 
