@@ -11,12 +11,14 @@
 // warp order and rounded once; TensorRT-LLM PR #20502, glmFusedAGemm commit
 // message -- re-drawn for bulk-copy rings and clusters on sm_103a):
 //
-//   * warp kNCW (the producer) fills a ring of shared-memory stages with 1-D bulk
-//     copies: one copy per weight row and per token row, each a contiguous
-//     segment of stage_units * 128 bytes (long contiguous reads keep DRAM pages
-//     open; 128-byte pieces at the row pitch do not).  The weight copies of the
-//     first ring's worth of stages are issued before griddepcontrol.wait, the
-//     activation copies only after it;
+//   * a ring of shared-memory stages is filled with 1-D bulk copies: one copy per
+//     weight row and per token row, each a contiguous segment of stage_units * 128
+//     bytes (long contiguous reads keep DRAM pages open; 128-byte pieces at the
+//     row pitch do not).  All nine warps issue copies -- warp w the rows and
+//     tokens congruent to w mod 9 -- because one issuing thread manages only about
+//     one copy per 55 ns.  The weight copies of the first ring's worth of stages
+//     are issued before griddepcontrol.wait, the activation copies only after
+//     it; a slot is refilled by the same warps once every consumer has released it;
 //   * shared rows are padded to a pitch of 16 mod 128 bytes, so the eight rows
 //     an ldmatrix phase reads fall in eight different bank groups;
 //   * consumer warp (wr, wk) takes every k-unit u (128 bytes of K) of a stage
@@ -57,7 +59,8 @@ template <int COMPUTE, int MT, int RT, int WR, int WK>
 struct StreamCfg {
     static constexpr int kCompute = COMPUTE;
     static constexpr int kNCW = WR * WK;                 // consumer warps
-    static constexpr int kThreads = (kNCW + 1) * 32;     // + producer warp
+    static constexpr int kNW = kNCW + 1;                 // + one issue-only warp
+    static constexpr int kThreads = kNW * 32;
     static constexpr int kSlots = WR * RT * 16;          // row slots per CTA
     static constexpr int kXRows = 8 * MT;                // token slots
     static_assert(WR * WK == 8, "eight consumer warps");
@@ -107,42 +110,63 @@ struct StageView {
 // ---- inner products on one 128-byte k-unit at byte offset `ub` of the stage ----
 
 // Tensor cores: 4 k-steps (k16 for bf16, k8 for tf32) over the warp's row tiles.
-template <class C, int RT, int MT>
+// All fragment loads of a batch of k-steps are issued before its products, so
+// their shared-memory latencies overlap (the whole unit for up to two token
+// tiles, two k-steps at a time for more).  With one token tile (M <= 8) the even
+// and odd k-steps feed two accumulator chains (acc[0], acc[1]) that are added at
+// the end: half the dependent MMA latency.  With more token tiles the tiles
+// themselves are independent chains.
+template <class C, int RT, int MT, int NCH>
 __device__ __forceinline__ void unit_mma(const StageView &v, uint32_t ub, int wr, int lane,
-                                         float (&acc)[RT][MT][4]) {
+                                         float (&acc)[NCH][RT][MT][4]) {
+    constexpr int kBatch = (MT >= 4) ? 2 : 4;
+    constexpr int kMask = NCH - 1;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-        uint32_t b[MT][2];
-        const uint32_t bb = ub + ks * 32 + ((lane >> 3) & 1) * 16;
-        if constexpr (MT == 1) {
-            ldsm_x2(v.xrow(lane & 7) + bb, b[0][0], b[0][1]);
-        } else {
+    for (int k0 = 0; k0 < 4; k0 += kBatch) {
+        uint32_t b[kBatch][MT][2];
+        uint32_t a[kBatch][RT][4];
 #pragma unroll
-            for (int j = 0; j < MT; j += 2) {
-                const int tok = (j + (lane >> 4)) * 8 + (lane & 7);
-                ldsm_x4(v.xrow(tok) + bb, b[j][0], b[j][1], b[j + 1][0], b[j + 1][1]);
-            }
-        }
-        if constexpr (C::kCompute == kMmaTf32) {
-#pragma unroll
-            for (int j = 0; j < MT; ++j) {
-                b[j][0] = to_tf32(b[j][0]);
-                b[j][1] = to_tf32(b[j][1]);
-            }
-        }
-        const uint32_t ab = ub + ks * 32 + (lane >> 4) * 16;
-#pragma unroll
-        for (int t = 0; t < RT; ++t) {
-            uint32_t a[4];
-            ldsm_x4(v.wrow(wr * RT * 16 + t * 16 + (lane & 15)) + ab, a[0], a[1], a[2], a[3]);
-            if constexpr (C::kCompute == kMmaTf32) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) a[q] = to_tf32(a[q]);
-#pragma unroll
-                for (int j = 0; j < MT; ++j) mma_tf32_1688(acc[t][j], a, b[j][0], b[j][1]);
+        for (int q = 0; q < kBatch; ++q) {
+            const uint32_t bb = ub + (k0 + q) * 32 + ((lane >> 3) & 1) * 16;
+            if constexpr (MT == 1) {
+                ldsm_x2(v.xrow(lane & 7) + bb, b[q][0][0], b[q][0][1]);
             } else {
 #pragma unroll
-                for (int j = 0; j < MT; ++j) mma_bf16_16816(acc[t][j], a, b[j][0], b[j][1]);
+                for (int j = 0; j < MT; j += 2) {
+                    const int tok = (j + (lane >> 4)) * 8 + (lane & 7);
+                    ldsm_x4(v.xrow(tok) + bb, b[q][j][0], b[q][j][1], b[q][j + 1][0], b[q][j + 1][1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const uint32_t ab = ub + (k0 + q) * 32 + (lane >> 4) * 16;
+#pragma unroll
+            for (int t = 0; t < RT; ++t)
+                ldsm_x4(v.wrow(wr * RT * 16 + t * 16 + (lane & 15)) + ab, a[q][t][0], a[q][t][1], a[q][t][2],
+                        a[q][t][3]);
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int ks = k0 + q;
+            if constexpr (C::kCompute == kMmaTf32) {
+#pragma unroll
+                for (int j = 0; j < MT; ++j) {
+                    b[q][j][0] = to_tf32(b[q][j][0]);
+                    b[q][j][1] = to_tf32(b[q][j][1]);
+                }
+#pragma unroll
+                for (int t = 0; t < RT; ++t) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) a[q][t][e] = to_tf32(a[q][t][e]);
+#pragma unroll
+                    for (int j = 0; j < MT; ++j) mma_tf32_1688(acc[ks & kMask][t][j], a[q][t], b[q][j][0], b[q][j][1]);
+                }
+            } else {
+#pragma unroll
+                for (int t = 0; t < RT; ++t)
+#pragma unroll
+                    for (int j = 0; j < MT; ++j) mma_bf16_16816(acc[ks & kMask][t][j], a[q][t], b[q][j][0], b[q][j][1]);
             }
         }
     }
@@ -256,7 +280,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
 
     if (tid == 0) {
         for (int s = 0; s < a.ring_stages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&full[s]), C::kNW);
             mbar_init(smem_u32(&empty[s]), C::kNCW);
             armed[s] = -1;
         }
@@ -265,86 +289,75 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     }
     __syncthreads();
 
-    float acc_mma[(COMPUTE == kFmaFp32) ? 1 : RT][(COMPUTE == kFmaFp32) ? 1 : MT][4];
+    constexpr int kChains = (COMPUTE != kFmaFp32 && MT == 1) ? 2 : 1;
+    float acc_mma[kChains][(COMPUTE == kFmaFp32) ? 1 : RT][(COMPUTE == kFmaFp32) ? 1 : MT][4];
     float acc_fk[(COMPUTE == kFmaFp32 && MT == 1) ? 4 * RT : 1][8];
     float acc_fo[(COMPUTE == kFmaFp32 && MT > 1) ? 4 * RT : 1][MT];
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(acc_mma) / sizeof(float)); ++i) (&acc_mma[0][0][0])[i] = 0.f;
+    for (int i = 0; i < (int)(sizeof(acc_mma) / sizeof(float)); ++i) (&acc_mma[0][0][0][0])[i] = 0.f;
 #pragma unroll
     for (int i = 0; i < (int)(sizeof(acc_fk) / sizeof(float)); ++i) (&acc_fk[0][0])[i] = 0.f;
 #pragma unroll
     for (int i = 0; i < (int)(sizeof(acc_fo) / sizeof(float)); ++i) (&acc_fo[0][0])[i] = 0.f;
 
-    if (warp == C::kNCW) {
-        // ---------------- producer ----------------
-        if (lane == 0) {
-            const uint64_t w_policy = l2_policy_evict_first();
-            const char *wrow0 = a.w + static_cast<int64_t>(row0) * a.row_bytes;
-            auto span = [&](int i, int64_t &byte0, uint32_t &nbytes) {
-                const int u0 = u_slice0 + i * a.stage_units;
-                const int u1 = min(u0 + a.stage_units, u_slice1);
-                byte0 = static_cast<int64_t>(u0) * kUnitBytes;
-                const int64_t end = min(static_cast<int64_t>(u1) * kUnitBytes, a.row_bytes);
-                nbytes = static_cast<uint32_t>(end - byte0);
-            };
-            auto issue_w = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
-                const uint32_t base = ring + slot * a.stage_bytes;
-                for (int r = 0; r < rows_here; ++r)
-                    bulk_load_hint(base + r * a.pitch, wrow0 + r * a.row_bytes + byte0, nbytes, fb, w_policy);
-            };
-            auto issue_x = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
-                const uint32_t base = ring + slot * a.stage_bytes + a.rows_per_cta * a.pitch;
-                for (int t = 0; t < a.M; ++t) bulk_load(base + t * a.pitch, a.x + t * a.row_bytes + byte0, nbytes, fb);
-            };
-            const int npre = min(nst, a.ring_stages);
-            // Weights of the first ring's worth of stages: before the grid dependency.
-            for (int i = 0; i < npre; ++i) {
-                if (i == a.skip_stage) continue;
-                int64_t b0;
-                uint32_t nb;
-                span(i, b0, nb);
-                const uint32_t fb = smem_u32(&full[i]);
-                mbar_expect_tx(fb, static_cast<uint32_t>(rows_here) * nb);
-                issue_w(i, b0, nb, fb);
-            }
-            // Activations are written by the previous kernel on the stream.
-            griddep_wait();
-            for (int i = 0; i < npre; ++i) {
-                if (i == a.skip_stage) continue;
-                int64_t b0;
-                uint32_t nb;
-                span(i, b0, nb);
-                const uint32_t fb = smem_u32(&full[i]);
-                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(a.M) * nb);
-                issue_x(i, b0, nb, fb);
-                armed[i] = i;
-            }
-            for (int i = npre; i < nst; ++i) {
-                const int slot = i % a.ring_stages;
-                const uint32_t par = static_cast<uint32_t>((i / a.ring_stages) - 1) & 1u;
-                if (!thread_wait(smem_u32(&empty[slot]), par, a.wait_limit_ns, abort_flag)) {
-                    record_timeout(a.err_word, abort_flag);
-                    break;
-                }
-                if (i == a.skip_stage) continue;
-                int64_t b0;
-                uint32_t nb;
-                span(i, b0, nb);
-                const uint32_t fb = smem_u32(&full[slot]);
-                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows_here + a.M) * nb);
-                issue_w(slot, b0, nb, fb);
-                issue_x(slot, b0, nb, fb);
-                armed[slot] = i;
-            }
+    // ---------------- copy issue (every warp, lane 0) ----------------
+    // Warp `warp` copies weight rows r = warp, warp + 9, ... and token rows
+    // t = warp, warp + 9, ... of every stage, and arrives once per stage phase.
+    const uint64_t w_policy = l2_policy_evict_first();
+    const char *wrow0 = a.w + static_cast<int64_t>(row0) * a.row_bytes;
+    auto span = [&](int i, int64_t &byte0, uint32_t &nbytes) {
+        const int u0 = u_slice0 + i * a.stage_units;
+        const int u1 = min(u0 + a.stage_units, u_slice1);
+        byte0 = static_cast<int64_t>(u0) * kUnitBytes;
+        const int64_t end = min(static_cast<int64_t>(u1) * kUnitBytes, a.row_bytes);
+        nbytes = static_cast<uint32_t>(end - byte0);
+    };
+    const int my_rows = rows_here > warp ? (rows_here - warp + C::kNW - 1) / C::kNW : 0;
+    const int my_toks = a.M > warp ? (a.M - warp + C::kNW - 1) / C::kNW : 0;
+    auto issue_w = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
+        const uint32_t base = ring + slot * a.stage_bytes;
+        for (int r = warp; r < rows_here; r += C::kNW)
+            bulk_load_hint(base + r * a.pitch, wrow0 + r * a.row_bytes + byte0, nbytes, fb, w_policy);
+    };
+    auto issue_x = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
+        const uint32_t base = ring + slot * a.stage_bytes + a.rows_per_cta * a.pitch;
+        for (int t = warp; t < a.M; t += C::kNW) bulk_load(base + t * a.pitch, a.x + t * a.row_bytes + byte0, nbytes, fb);
+    };
+    const int npre = min(nst, a.ring_stages);
+    if (lane == 0) {
+        // Weights of the first ring's worth of stages: before the grid dependency.
+        for (int i = 0; i < npre; ++i) {
+            if (i == a.skip_stage) continue;
+            int64_t b0;
+            uint32_t nb;
+            span(i, b0, nb);
+            if (my_rows > 0) mbar_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_rows) * nb);
+            issue_w(i, b0, nb, smem_u32(&full[i]));
         }
-        __syncwarp();
-    } else {
-        // ---------------- consumers ----------------
-        const int wk = warp % WK, wr = warp / WK;
-        const bool has_rows = wr * RT * 16 < rows_here;
-        for (int i = 0; i < nst; ++i) {
-            const int slot = i % a.ring_stages;
-            const uint32_t par = static_cast<uint32_t>(i / a.ring_stages) & 1u;
+    }
+    // Activations are written by the previous kernel on the stream.
+    griddep_wait();
+    if (lane == 0) {
+        for (int i = 0; i < npre; ++i) {
+            if (i == a.skip_stage) continue;
+            int64_t b0;
+            uint32_t nb;
+            span(i, b0, nb);
+            mbar_arrive_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_toks) * nb);
+            issue_x(i, b0, nb, smem_u32(&full[i]));
+            if (warp == 0) armed[i] = i;
+        }
+    }
+    __syncwarp();
+
+    // ---------------- consume stage i, then refill its slot with stage i + ring ----------------
+    const int wk = warp % WK, wr = warp / WK;
+    const bool consumer = warp < C::kNCW;
+    const bool has_rows = consumer && wr * RT * 16 < rows_here;
+    for (int i = 0; i < nst; ++i) {
+        const int slot = i % a.ring_stages;
+        const uint32_t par = static_cast<uint32_t>(i / a.ring_stages) & 1u;
+        if (consumer) {
             if (!warp_wait(smem_u32(&full[slot]), par, a.wait_limit_ns, abort_flag)) {
                 if (lane == 0) record_timeout(a.err_word, abort_flag);
                 break;
@@ -359,8 +372,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             v.tmax = a.M - 1;
             bool zeroed = false;
             // units of this warp: u = u0 + j with u mod WK == wk, in increasing order
-            int u = u0 + ((wk - u0 % WK) % WK + WK) % WK;
-            for (; u < u1; u += WK) {
+            for (int u = u0 + ((wk - u0 % WK) % WK + WK) % WK; u < u1; u += WK) {
                 const uint32_t ub = static_cast<uint32_t>(u - u0) * kUnitBytes;
                 const int64_t valid = a.row_bytes - static_cast<int64_t>(u) * kUnitBytes;
                 if (valid < kUnitBytes) {
@@ -374,12 +386,30 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                     else
                         unit_fma_outer<C, RT, MT>(v, ub, wr, lane, acc_fo);
                 } else {
-                    unit_mma<C, RT, MT>(v, ub, wr, lane, acc_mma);
+                    unit_mma<C, RT, MT, kChains>(v, ub, wr, lane, acc_mma);
                 }
             }
             if (zeroed) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+        }
+        const int j = i + a.ring_stages;
+        if (j < nst) {
+            // every consumer has released the slot: issue this warp's share of stage j
+            if (!warp_wait(smem_u32(&empty[slot]), par, a.wait_limit_ns, abort_flag)) {
+                if (lane == 0) record_timeout(a.err_word, abort_flag);
+                break;
+            }
+            if (lane == 0 && j != a.skip_stage) {
+                int64_t b0;
+                uint32_t nb;
+                span(j, b0, nb);
+                mbar_arrive_expect_tx(smem_u32(&full[slot]), static_cast<uint32_t>(my_rows + my_toks) * nb);
+                issue_w(slot, b0, nb, smem_u32(&full[slot]));
+                issue_x(slot, b0, nb, smem_u32(&full[slot]));
+                if (warp == 0) armed[slot] = j;
+            }
+            __syncwarp();
         }
     }
 
@@ -388,7 +418,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     const bool aborted = (*abort_flag != 0);
     if (aborted) {
         // Let copies still in flight land before the ring is reused or freed.
-        if (warp == C::kNCW && lane == 0) {
+        if (warp == 0 && lane == 0) {
             const uint64_t limit = a.wait_limit_ns / 16 + 1;
             for (int s = 0; s < a.ring_stages; ++s) {
                 const int i = armed[s];
@@ -436,10 +466,16 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                     const int t0 = j * 8 + 2 * (lane & 3);
                     float *p0 = red + (wk * kSlots + s0) * kXRows + t0;
                     float *p1 = red + (wk * kSlots + s0 + 8) * kXRows + t0;
-                    p0[0] = acc_mma[t][j][0];
-                    p0[1] = acc_mma[t][j][1];
-                    p1[0] = acc_mma[t][j][2];
-                    p1[1] = acc_mma[t][j][3];
+                    float d[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        d[q] = acc_mma[0][t][j][q];
+                        if constexpr (kChains == 2) d[q] += acc_mma[kChains - 1][t][j][q];
+                    }
+                    p0[0] = d[0];
+                    p0[1] = d[1];
+                    p1[0] = d[2];
+                    p1[1] = d[3];
                 }
         }
     }
@@ -449,6 +485,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     griddep_wait();
 
     // ---- warp partials added in warp order; single-slice CTAs store here ----
+    bool stored = false;
     if (!aborted) {
         for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
             const int tok = e / kSlots, slot = e - tok * kSlots;
@@ -456,10 +493,12 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             float v = red[slot * kXRows + tok];
 #pragma unroll
             for (int q = 1; q < WK; ++q) v += red[(q * kSlots + slot) * kXRows + tok];
-            if (a.slices == 1)
+            if (a.slices == 1) {
                 store_out<COMPUTE>(a, row0 + slot, tok, v);
-            else
+                stored = true;
+            } else {
                 red[slot * kXRows + tok] = v;
+            }
         }
     }
 
@@ -477,13 +516,15 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 for (int q = 1; q < a.slices; ++q)
                     v += ld_shared_cluster_f32(cluster_map_shared(off, static_cast<uint32_t>(q)));
                 store_out<COMPUTE>(a, row0 + slot, tok, v);
+                stored = true;
             }
         }
         cluster_sync_all();  // no CTA leaves while a peer may still read its partials
     }
 
-    // Trigger the dependent launch only after every output store of this CTA.
-    __threadfence();
+    // Trigger the dependent launch only after every output store of this CTA is
+    // performed: each storing thread fences, then the CTA synchronises.
+    if (stored) fence_release_gpu();
     __syncthreads();
     griddep_launch_dependents();
 }
