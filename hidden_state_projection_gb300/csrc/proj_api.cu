@@ -75,7 +75,36 @@ struct DeviceInfo {
     int sms = 0;
     int cc_ok = 0;
     int *err_word = nullptr;
+    int cluster_ctas[5] = {0, 0, 0, 0, 0};  // CTAs co-resident in clusters of 1, 2, 4 (index = size)
 };
+
+// Shape of the streaming kernels for the co-residency query: one CTA of 288
+// threads and ~200 KB of shared memory per SM.
+__global__ void hsp_cluster_probe_kernel(int *p) {
+    if (p && threadIdx.x == 0x7fffffff) p[0] = 1;
+}
+
+int co_resident_ctas(int cluster, int fallback) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, static_cast<unsigned>(cluster * 16), 1);
+    cfg.blockDim = dim3(288, 1, 1);
+    cfg.dynamicSmemBytes = 200 * 1024;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = static_cast<unsigned>(cluster);
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaFuncSetAttribute(hsp_cluster_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, hsp_cluster_probe_kernel, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
+    return n * cluster;
+}
 
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
@@ -95,7 +124,10 @@ proj_status device_info(DeviceInfo *out) {
             (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
         d.cc_ok = (major == 10 && minor == 3);
+        d.cluster_ctas[1] = d.sms;
         if (d.cc_ok) {
+            d.cluster_ctas[2] = co_resident_ctas(2, d.sms);
+            d.cluster_ctas[4] = co_resident_ctas(4, d.sms);
             void *p = nullptr;
             if ((e = cudaGetSymbolAddress(&p, g_hsp_device_error)) != cudaSuccess)
                 return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
@@ -140,7 +172,7 @@ proj_status check_shape(int32_t M, int32_t K, int64_t n_total, int dt) {
 //   - R (rows per CTA) spreads the rows over the SMs and the stage width is the
 //     widest that still leaves two ring stages in shared memory: long contiguous
 //     row segments per bulk copy.  Neither changes the order.
-void make_plan(int M, int K, int n_rows, proj_dtype dt, int sms, Plan *p) {
+void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas, Plan *p) {
     memset(p, 0, sizeof *p);
     const int esz = elem_size(dt);
     p->compute = dt == PROJ_BF16 ? hsp::kMmaBf16 : (dt == PROJ_TF32 ? hsp::kMmaTf32 : hsp::kFmaFp32);
@@ -165,7 +197,10 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, int sms, Plan *p) {
         p->units_per_slice = ceil_div(ceil_div(p->units_total, p->S), p->WK) * p->WK;
     }
     const int max_rows = p->WR * 2 * 16;
-    p->R = p->bucket == 0 ? ceil_div(n_rows, sms) : ceil_div(n_rows * p->S, sms);
+    // rows per CTA: spread over the CTAs that can be resident at once (clusters of
+    // S leave some SMs of a GPC idle)
+    const int resident = cluster_ctas[p->S] > 0 ? cluster_ctas[p->S] : cluster_ctas[1];
+    p->R = ceil_div(n_rows * p->S, resident);
     if (p->R < 1) p->R = 1;
     if (p->R > max_rows) p->R = max_rows;
     p->RT = p->R > p->WR * 16 ? 2 : 1;
@@ -220,7 +255,7 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, int sms, Plan *p) {
 proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
                         proj_dtype dt, const hsp::SplitTable &splits, cudaStream_t stream) {
     Plan p;
-    make_plan(M, K, n_rows, dt, dev.sms, &p);
+    make_plan(M, K, n_rows, dt, dev.cluster_ctas, &p);
     if (p.ring_stages < 1 || p.smem > kSmemLimit)
         return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "no shared-memory plan for M=%d K=%d rows=%d", M, K, n_rows);
     LaunchReq r{};
@@ -385,16 +420,21 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
     proj_status st = check_shape(M, K, n_rows, dtype);
     if (st != PROJ_OK) return st;
     if (M < 1 || n_rows < 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "M and n_rows must be at least 1");
-    int sms = 152;
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
-    } else {
-        (void)cudaGetLastError();
+    // Without a usable device the plan assumes a GB300: 152 SMs, 152 / 152 / 144
+    // CTAs co-resident in clusters of 1 / 2 / 4.
+    int ctas[5] = {0, 152, 152, 0, 144};
+    {
+        char saved[sizeof g_last_error];
+        memcpy(saved, g_last_error, sizeof saved);
+        DeviceInfo d;
+        if (device_info(&d) == PROJ_OK)
+            for (int k = 1; k < 5; ++k) ctas[k] = d.cluster_ctas[k];
+        else
+            (void)cudaGetLastError();
+        memcpy(g_last_error, saved, sizeof saved);
     }
     Plan p;
-    make_plan(M, K, n_rows, dtype, sms, &p);
+    make_plan(M, K, n_rows, dtype, ctas, &p);
     *info = p.info;
     return ok();
 }

@@ -15,8 +15,8 @@
 //     weight row and per token row, each a contiguous segment of stage_units * 128
 //     bytes (long contiguous reads keep DRAM pages open; 128-byte pieces at the
 //     row pitch do not).  All nine warps issue copies -- warp w the rows and
-//     tokens congruent to w mod 9 -- because one issuing thread manages only about
-//     one copy per 55 ns.  The weight copies of the first ring's worth of stages
+//     tokens congruent to w mod 9, one lane per copy -- because one issuing
+//     thread manages only about one copy per 55-150 ns.  The weight copies of the first ring's worth of stages
 //     are issued before griddepcontrol.wait, the activation copies only after
 //     it; a slot is refilled by the same warps once every consumer has released it;
 //   * shared rows are padded to a pitch of 16 mod 128 bytes, so the eight rows
@@ -300,9 +300,10 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
 #pragma unroll
     for (int i = 0; i < (int)(sizeof(acc_fo) / sizeof(float)); ++i) (&acc_fo[0][0])[i] = 0.f;
 
-    // ---------------- copy issue (every warp, lane 0) ----------------
-    // Warp `warp` copies weight rows r = warp, warp + 9, ... and token rows
-    // t = warp, warp + 9, ... of every stage, and arrives once per stage phase.
+    // ---------------- copy issue (every warp, lane-parallel) ----------------
+    // Warp `warp` copies weight rows r = warp + 9 l and token rows t = warp + 9 l;
+    // lane l issues the copy of its row, after lane 0 has raised the stage's
+    // expected byte count by the warp's share.  Each warp arrives once per phase.
     const uint64_t w_policy = l2_policy_evict_first();
     const char *wrow0 = a.w + static_cast<int64_t>(row0) * a.row_bytes;
     auto span = [&](int i, int64_t &byte0, uint32_t &nbytes) {
@@ -314,39 +315,46 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     };
     const int my_rows = rows_here > warp ? (rows_here - warp + C::kNW - 1) / C::kNW : 0;
     const int my_toks = a.M > warp ? (a.M - warp + C::kNW - 1) / C::kNW : 0;
+    // lane-parallel issue of this warp's rows (and tokens) of one stage; lanes past
+    // 32 loop (a CTA has at most 128 rows and 64 tokens)
     auto issue_w = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
         const uint32_t base = ring + slot * a.stage_bytes;
-        for (int r = warp; r < rows_here; r += C::kNW)
+        for (int l = lane; l < my_rows; l += 32) {
+            const int r = warp + C::kNW * l;
             bulk_load_hint(base + r * a.pitch, wrow0 + r * a.row_bytes + byte0, nbytes, fb, w_policy);
+        }
     };
     auto issue_x = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
         const uint32_t base = ring + slot * a.stage_bytes + a.rows_per_cta * a.pitch;
-        for (int t = warp; t < a.M; t += C::kNW) bulk_load(base + t * a.pitch, a.x + t * a.row_bytes + byte0, nbytes, fb);
+        for (int l = lane; l < my_toks; l += 32) {
+            const int t = warp + C::kNW * l;
+            bulk_load(base + t * a.pitch, a.x + t * a.row_bytes + byte0, nbytes, fb);
+        }
     };
     const int npre = min(nst, a.ring_stages);
-    if (lane == 0) {
-        // Weights of the first ring's worth of stages: before the grid dependency.
-        for (int i = 0; i < npre; ++i) {
-            if (i == a.skip_stage) continue;
-            int64_t b0;
-            uint32_t nb;
-            span(i, b0, nb);
-            if (my_rows > 0) mbar_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_rows) * nb);
-            issue_w(i, b0, nb, smem_u32(&full[i]));
-        }
+    // Weights of the first ring's worth of stages: before the grid dependency.
+    for (int i = 0; i < npre; ++i) {
+        if (i == a.skip_stage) continue;
+        int64_t b0;
+        uint32_t nb;
+        span(i, b0, nb);
+        if (lane == 0 && my_rows > 0) mbar_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_rows) * nb);
+        __syncwarp();
+        issue_w(i, b0, nb, smem_u32(&full[i]));
     }
     // Activations are written by the previous kernel on the stream.
     griddep_wait();
-    if (lane == 0) {
-        for (int i = 0; i < npre; ++i) {
-            if (i == a.skip_stage) continue;
-            int64_t b0;
-            uint32_t nb;
-            span(i, b0, nb);
+    for (int i = 0; i < npre; ++i) {
+        if (i == a.skip_stage) continue;
+        int64_t b0;
+        uint32_t nb;
+        span(i, b0, nb);
+        if (lane == 0) {
             mbar_arrive_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_toks) * nb);
-            issue_x(i, b0, nb, smem_u32(&full[i]));
             if (warp == 0) armed[i] = i;
         }
+        __syncwarp();
+        issue_x(i, b0, nb, smem_u32(&full[i]));
     }
     __syncwarp();
 
@@ -400,14 +408,17 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 if (lane == 0) record_timeout(a.err_word, abort_flag);
                 break;
             }
-            if (lane == 0 && j != a.skip_stage) {
+            if (j != a.skip_stage) {
                 int64_t b0;
                 uint32_t nb;
                 span(j, b0, nb);
-                mbar_arrive_expect_tx(smem_u32(&full[slot]), static_cast<uint32_t>(my_rows + my_toks) * nb);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(smem_u32(&full[slot]), static_cast<uint32_t>(my_rows + my_toks) * nb);
+                    if (warp == 0) armed[slot] = j;
+                }
+                __syncwarp();
                 issue_w(slot, b0, nb, smem_u32(&full[slot]));
                 issue_x(slot, b0, nb, smem_u32(&full[slot]));
-                if (warp == 0) armed[slot] = j;
             }
             __syncwarp();
         }
