@@ -48,6 +48,39 @@ def dist_env():
     return ws, rank, local
 
 
+def kernel_sources_sha16():
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "hidden_state_projection_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu"))) + sorted(glob.glob(os.path.join(csrc, "*.cuh"))) \
+        + sorted(glob.glob(os.path.join(csrc, "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, M):
+    """DRAM bytes per launch from the committed ncu summary of this workload, if that
+    summary was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"hsp_stream_kernel_{name}_m{M}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith(("#", "|", " ")):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("kernel_sources_sha256_16") != kernel_sources_sha16():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -290,7 +323,8 @@ def run_ours(args):
             "pdl": not args.no_pdl, "parallelism": f"replicas x{ws}",
         },
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": args.traffic if args.traffic is not None else profiled_traffic(name, M),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "bytes_per_call": bytes_call, "us_per_call": round(us_call, 4)},
