@@ -44,14 +44,15 @@ class ProjError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("pdl", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
-                ("skip_stage_plus1", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("skip_stage_plus1", ctypes.c_int32), ("large_m_path", ctypes.c_int32),
+                ("l2_prefetch", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "bucket", "compute", "rows_per_cta", "row_ctas", "slices", "k_warps", "row_warps",
         "row_tiles", "token_tiles", "ring_stages", "stage_bytes", "smem_bytes", "k_per_stage",
-        "stages_total", "threads", "units_per_slice")] + [("reserved", ctypes.c_int32 * 4)]
+        "stages_total", "threads", "units_per_slice", "engine")] + [("reserved", ctypes.c_int32 * 3)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}
@@ -209,18 +210,22 @@ def describe_plan(M: int, K: int, n_rows: int, dtype: int) -> dict:
     return info.as_dict()
 
 
-def set_options(pdl: Optional[bool] = None, wait_limit_us: int = 0, skip_stage: Optional[int] = None):
+def set_options(pdl: Optional[bool] = None, wait_limit_us: int = 0, skip_stage: Optional[int] = None,
+                large_m_path: int = 0, l2_prefetch: bool = False):
     o = Options()
     o.pdl = -1 if pdl is None else int(bool(pdl))
     o.wait_limit_us = int(wait_limit_us)
     o.skip_stage_plus1 = 0 if skip_stage is None else int(skip_stage) + 1
+    o.large_m_path = int(large_m_path)
+    o.l2_prefetch = 1 if l2_prefetch else 0
     _check(lib().proj_set_options(ctypes.byref(o)))
 
 
 def get_options() -> dict:
     o = Options()
     _check(lib().proj_get_options(ctypes.byref(o)))
-    return {"pdl": o.pdl, "wait_limit_us": o.wait_limit_us, "skip_stage_plus1": o.skip_stage_plus1}
+    return {"pdl": o.pdl, "wait_limit_us": o.wait_limit_us, "skip_stage_plus1": o.skip_stage_plus1,
+            "large_m_path": o.large_m_path, "l2_prefetch": o.l2_prefetch}
 
 
 def check_device_error(stream=None) -> None:

@@ -1,6 +1,7 @@
 // launch.h -- host-side launch request for the streaming kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "stream_args.h"
@@ -24,7 +25,22 @@ cudaError_t launch_bf16(const LaunchReq &r);
 cudaError_t launch_tf32(const LaunchReq &r);
 cudaError_t launch_fp32(const LaunchReq &r);
 
+// Tensor-memory kernel launch (9 <= M <= 64).
+struct UmmaLaunchReq {
+    int compute;     // kMmaBf16 or kMmaTf32
+    int NT;          // token tile: 16, 32 or 64
+    dim3 grid;       // (128-row tiles, slices, 1)
+    int smem_bytes;
+    int pdl;
+    cudaStream_t stream;
+    CUtensorMap tmap_w;
+    CUtensorMap tmap_x;
+    UmmaArgs args;
+};
+cudaError_t launch_umma(const UmmaLaunchReq &r);
+
 // Threads per CTA of a bucket (eight consumer warps + one producer warp).
 constexpr int kThreadsPerCta = 9 * 32;
+constexpr int kUmmaThreadsHost = 128;
 
 }  // namespace hsp

@@ -12,7 +12,9 @@
 // bucket) only, so an output row is summed in the same order whatever the
 // number of rows in the launch -- the property that makes the fused and the
 // separate calls bitwise equal.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cstdarg>
@@ -39,6 +41,8 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_opt_pdl{1};
 std::atomic<int> g_opt_wait_us{0};
 std::atomic<int> g_opt_skip_stage_plus1{0};
+std::atomic<int> g_opt_large_m_path{0};
+std::atomic<int> g_opt_l2_prefetch{0};
 
 }  // namespace
 
@@ -206,7 +210,8 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     p->RT = p->R > p->WR * 16 ? 2 : 1;
     const int slots = p->WR * p->RT * 16;
     p->grid_x = ceil_div(n_rows, p->R);
-    const int red_bytes = p->WK * slots * 8 * p->MT * 4;
+    // partials of the warps, plus (K slices) the receive buffer of the cluster reduction
+    const int red_bytes = p->WK * slots * 8 * p->MT * 4 + (p->S > 1 ? slots * 8 * p->MT * 4 : 0);
     const int budget = kSmemLimit - kSmemReserve;
     const int Us = p->units_per_slice;
     const int first = Us >= 2 * p->WK ? 2 : 1;
@@ -251,9 +256,165 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     i.units_per_slice = p->units_per_slice;
 }
 
+// ---- tensor maps (tensor-memory kernel only) ---------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct MapEntry {
+    uint64_t ptr, d0, d1, box0, box1;
+    int dtype;
+    bool used;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 256;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+// 2-D map over a row-major [d1, d0] matrix (d0 contiguous), box [box1 rows, box0
+// elements] = 128 bytes wide, 128-byte swizzle, zero fill outside the matrix.
+proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0, uint32_t box1, proj_dtype dt,
+                       CUtensorMap *out) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            (void)cudaGetLastError();
+    });
+    if (!g_encode) return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const uint64_t key = reinterpret_cast<uint64_t>(ptr);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        for (int i = 0; i < kMapCache; ++i) {
+            const MapEntry &m = g_maps[i];
+            if (m.used && m.ptr == key && m.d0 == d0 && m.d1 == d1 && m.box0 == box0 && m.box1 == box1 &&
+                m.dtype == static_cast<int>(dt)) {
+                *out = m.map;
+                return PROJ_OK;
+            }
+        }
+    }
+    CUtensorMap map;
+    cuuint64_t dims[2] = {d0, d1};
+    cuuint64_t strides[1] = {d0 * static_cast<uint64_t>(elem_size(dt))};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&map, dt == PROJ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu], box [%u x %u]",
+                    static_cast<int>(r), (unsigned long long)d1, (unsigned long long)d0, box1, box0);
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        g_maps[g_map_next] = MapEntry{key, d0, d1, box0, box1, static_cast<int>(dt), true, map};
+        g_map_next = (g_map_next + 1) % kMapCache;
+    }
+    *out = map;
+    return PROJ_OK;
+}
+
+// ---- tensor-memory plan ----------------------------------------------------
+
+bool use_umma(int M, proj_dtype dt) { return M > 8 && dt == PROJ_BF16 && g_opt_large_m_path.load() == 0; }
+
+struct UPlan {
+    proj_plan_info info;
+    int compute, NT, S, kb_total, kb_per_slice, tiles, ring, stage_bytes, x_box, smem;
+};
+
+// K slices and k-blocks per slice depend on (K, dtype) only; the ring is sized
+// so that two CTAs fit on an SM (clusters of eight then pack into the GPCs).
+void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, UPlan *p) {
+    memset(p, 0, sizeof *p);
+    const int64_t row_bytes = static_cast<int64_t>(K) * elem_size(dt);
+    p->compute = dt == PROJ_BF16 ? hsp::kMmaBf16 : hsp::kMmaTf32;
+    p->NT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    p->kb_total = static_cast<int>((row_bytes + 127) / 128);
+    p->S = p->kb_total >= 64 ? 8 : (p->kb_total >= 32 ? 4 : (p->kb_total >= 8 ? 2 : 1));
+    p->kb_per_slice = ceil_div(p->kb_total, p->S);
+    while (p->S > 1 && (p->S - 1) * p->kb_per_slice >= p->kb_total) {
+        --p->S;
+        p->kb_per_slice = ceil_div(p->kb_total, p->S);
+    }
+    p->tiles = ceil_div(n_rows, 128);
+    p->x_box = p->NT * 128;
+    p->stage_bytes = 16384 + p->x_box;
+    int ring = (110 * 1024) / p->stage_bytes;
+    if (ring < 2) ring = 2;
+    if (ring > p->kb_per_slice) ring = p->kb_per_slice < 2 ? 2 : p->kb_per_slice;
+    p->ring = ring;
+    p->smem = 1024 + ring * p->stage_bytes + (2 * ring + 1) * 8 + 16 + 64;
+    proj_plan_info &i = p->info;
+    i.bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
+    i.compute = p->compute;
+    i.rows_per_cta = 128;
+    i.row_ctas = p->tiles;
+    i.slices = p->S;
+    i.k_warps = 1;
+    i.row_warps = 4;
+    i.row_tiles = 1;
+    i.token_tiles = p->NT / 8;
+    i.ring_stages = p->ring;
+    i.stage_bytes = p->stage_bytes;
+    i.smem_bytes = p->smem;
+    i.k_per_stage = 128 / elem_size(dt);
+    i.stages_total = p->kb_per_slice;
+    i.threads = hsp::kUmmaThreadsHost;
+    i.units_per_slice = p->kb_per_slice;
+    i.engine = 1;
+}
+
+proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
+                             proj_dtype dt, const hsp::SplitTable &splits, cudaStream_t stream) {
+    UPlan p;
+    make_umma_plan(M, K, n_rows, dt, &p);
+    hsp::UmmaLaunchReq r{};
+    const uint32_t boxk = 128u / static_cast<uint32_t>(elem_size(dt));
+    proj_status st = encode_map(w, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), boxk, 128u, dt, &r.tmap_w);
+    if (st != PROJ_OK) return st;
+    st = encode_map(x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), boxk, static_cast<uint32_t>(p.NT), dt,
+                    &r.tmap_x);
+    if (st != PROJ_OK) return st;
+    r.compute = p.compute;
+    r.NT = p.NT;
+    r.grid = dim3(static_cast<unsigned>(p.tiles), static_cast<unsigned>(p.S), 1);
+    r.smem_bytes = p.smem;
+    r.pdl = g_opt_pdl.load();
+    r.stream = stream;
+    hsp::UmmaArgs &a = r.args;
+    a.w = static_cast<const char *>(w);
+    a.row_bytes = static_cast<int64_t>(K) * elem_size(dt);
+    a.n_rows = n_rows;
+    a.M = M;
+    a.kb_total = p.kb_total;
+    a.kb_per_slice = p.kb_per_slice;
+    a.slices = p.S;
+    a.ring_stages = p.ring;
+    a.stage_bytes = static_cast<uint32_t>(p.stage_bytes);
+    a.x_box_bytes = static_cast<uint32_t>(p.x_box);
+    a.prefetch_l2 = g_opt_l2_prefetch.load();
+    a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
+    const int wus = g_opt_wait_us.load();
+    a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
+    a.err_word = dev.err_word;
+    a.splits = splits;
+    cudaError_t e = hsp::launch_umma(r);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch (tensor-memory path)");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PROJ_OK;
+}
+
 // One launch over `n_rows` weight rows starting at `w` (already offset to the first row).
 proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
                         proj_dtype dt, const hsp::SplitTable &splits, cudaStream_t stream) {
+    if (use_umma(M, dt)) return launch_umma_rows(dev, x, w, n_rows, M, K, dt, splits, stream);
     Plan p;
     make_plan(M, K, n_rows, dt, dev.cluster_ctas, &p);
     if (p.ring_stages < 1 || p.smem > kSmemLimit)
@@ -433,6 +594,12 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
             (void)cudaGetLastError();
         memcpy(g_last_error, saved, sizeof saved);
     }
+    if (use_umma(M, dtype)) {
+        UPlan u;
+        make_umma_plan(M, K, n_rows, dtype, &u);
+        *info = u.info;
+        return ok();
+    }
     Plan p;
     make_plan(M, K, n_rows, dtype, ctas, &p);
     *info = p.info;
@@ -444,9 +611,13 @@ proj_status proj_set_options(const proj_options *opt) {
     if (opt->pdl < -1 || opt->pdl > 1) return fail(PROJ_ERR_INVALID_ARG, "pdl must be -1, 0 or 1");
     if (opt->wait_limit_us < 0 || opt->skip_stage_plus1 < 0)
         return fail(PROJ_ERR_INVALID_ARG, "wait_limit_us and skip_stage_plus1 must be >= 0");
+    if (opt->large_m_path < 0 || opt->large_m_path > 1 || opt->l2_prefetch < 0 || opt->l2_prefetch > 1)
+        return fail(PROJ_ERR_INVALID_ARG, "large_m_path and l2_prefetch must be 0 or 1");
     if (opt->pdl >= 0) g_opt_pdl.store(opt->pdl);
     g_opt_wait_us.store(opt->wait_limit_us);
     g_opt_skip_stage_plus1.store(opt->skip_stage_plus1);
+    g_opt_large_m_path.store(opt->large_m_path);
+    g_opt_l2_prefetch.store(opt->l2_prefetch);
     return ok();
 }
 
@@ -456,6 +627,8 @@ proj_status proj_get_options(proj_options *opt) {
     opt->pdl = g_opt_pdl.load();
     opt->wait_limit_us = g_opt_wait_us.load();
     opt->skip_stage_plus1 = g_opt_skip_stage_plus1.load();
+    opt->large_m_path = g_opt_large_m_path.load();
+    opt->l2_prefetch = g_opt_l2_prefetch.load();
     return ok();
 }
 

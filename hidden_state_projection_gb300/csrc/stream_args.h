@@ -49,4 +49,25 @@ struct StreamArgs {
     SplitTable splits;
 };
 
+// Tensor-memory path (9 <= M <= 64): a CTA owns a 128-row weight tile and one
+// K slice of `kb_per_slice` 128-byte k-blocks; the S slices of a row tile form a
+// cluster and add their partials in slice order.
+struct UmmaArgs {
+    const char *w;             // first weight row of the launch (for the L2 prefetch)
+    int64_t row_bytes;         // K * element size
+    int32_t n_rows;            // rows of the launch
+    int32_t M;                 // tokens
+    int32_t kb_total;          // ceil(row_bytes / 128)
+    int32_t kb_per_slice;      // k-blocks of one K slice
+    int32_t slices;            // S (cluster size along grid.y)
+    int32_t ring_stages;
+    uint32_t stage_bytes;      // 16384 (weight box) + x_box_bytes, a multiple of 1024
+    uint32_t x_box_bytes;      // token rows (16, 32 or 64) * 128
+    int32_t prefetch_l2;       // 1: bulk-prefetch the CTA's weight segments into L2 first
+    int32_t skip_stage;        // test hook: this k-block of every slice is never loaded (-1: off)
+    uint64_t wait_limit_ns;
+    int *err_word;
+    SplitTable splits;
+};
+
 }  // namespace hsp

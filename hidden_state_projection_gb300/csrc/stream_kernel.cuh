@@ -514,23 +514,38 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     }
 
     if (a.slices > 1) {
-        // ---- K slices of the cluster added in slice order (DSMEM) ----
+        // ---- K slices of the cluster added in slice order ----
+        // Push model: each CTA stores its combined partial P[slot][tok] into the
+        // receive buffer recv[slice][slot - owner*per][tok] of the CTA that owns the
+        // slot (remote stores do not wait); after the second cluster barrier each
+        // owner adds the S slices in slice order from its own shared memory.  recv
+        // sits after the partials in the ring, which every CTA has left once the
+        // first barrier is passed.
+        const int per = kSlots / a.slices;
+        float *recv = red + WK * kSlots * kXRows;
+        const uint32_t recv_local = smem_u32(recv);
         cluster_sync_all();
         if (!aborted) {
-            const int per = kSlots / a.slices;
-            const uint32_t red_local = smem_u32(red);
-            for (int e = tid; e < per * kXRows; e += C::kThreads) {
-                const int tok = e / per, slot = slice * per + (e - tok * per);
+            for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
+                const int slot = e / kXRows, tok = e - slot * kXRows;
                 if (tok >= a.M || slot >= rows_here) continue;
-                const uint32_t off = red_local + static_cast<uint32_t>((slot * kXRows + tok) * 4);
-                float v = ld_shared_cluster_f32(cluster_map_shared(off, 0));
-                for (int q = 1; q < a.slices; ++q)
-                    v += ld_shared_cluster_f32(cluster_map_shared(off, static_cast<uint32_t>(q)));
+                const int q = slot / per;
+                const uint32_t dst = recv_local + static_cast<uint32_t>(((slice * per + slot - q * per) * kXRows + tok) * 4);
+                st_shared_cluster_f32(cluster_map_shared(dst, static_cast<uint32_t>(q)), red[slot * kXRows + tok]);
+            }
+        }
+        cluster_sync_all();
+        if (!aborted) {
+            for (int e = tid; e < per * kXRows; e += C::kThreads) {
+                const int tok = e / per, rr = e - tok * per;
+                const int slot = slice * per + rr;
+                if (tok >= a.M || slot >= rows_here) continue;
+                float v = recv[rr * kXRows + tok];
+                for (int q = 1; q < a.slices; ++q) v += recv[(q * per + rr) * kXRows + tok];
                 store_out<COMPUTE>(a, row0 + slot, tok, v);
                 stored = true;
             }
         }
-        cluster_sync_all();  // no CTA leaves while a peer may still read its partials
     }
 
     // Trigger the dependent launch only after every output store of this CTA is

@@ -1,0 +1,300 @@
+// umma_kernel.cuh -- the tensor-memory (tcgen05) projection kernel for 9 <= M <= 64.
+//
+// Same operation and output scatter as the streaming kernel (TensorRT-LLM PR #20636,
+// Description), for the token counts where the products no longer fit the legacy
+// mma.sync issue rate.  One CTA of four warps owns a 128-row tile of the weight rows
+// and one K slice; its S K slices form a cluster.
+//
+//   * warps 2-3 first bulk-prefetch the CTA's weight segments (one contiguous run per
+//     row) into L2, so the DRAM sees long runs although the tensor copies below read
+//     128-byte pieces of 128 rows;
+//   * warp 0 lane 0 issues 2-D tensor copies (128-byte swizzle) of the weight box
+//     [128 rows x 128 bytes] and the token box [16/32/64 tokens x 128 bytes] of each
+//     k-block into a ring; weight boxes of the first ring's worth of k-blocks go out
+//     before griddepcontrol.wait, token boxes after it (the GLM fused-A order of
+//     TensorRT-LLM PR #20502, glmFusedAGemm commit message);
+//   * warp 1 lane 0 issues four tcgen05.mma (M = 128 weight rows, N = the token tile,
+//     K = 16 bf16 or 8 tf32 each) per k-block into one TMEM accumulator and commits
+//     each stage back to the ring; a final commit marks the accumulator ready;
+//   * all four warps read the accumulator (warp w owns TMEM lanes 32w..32w+31, one
+//     weight row per thread), then either store (S = 1) or push each row's partial
+//     into the shared memory of the CTA that owns the row (st.shared::cluster), and
+//     the owner adds the S slices in slice order and stores.  The sum of every
+//     output is the tensor-core accumulation over K in order, then slices in order:
+//     a function of (K, dtype, M bucket) only, never of the row's place in a tile.
+//   * the trigger follows a release fence in every storing thread (TensorRT-LLM PR
+//     #20636, Description).
+//
+// Rows past the launch, tokens past M and k past K are zero-filled by the tensor
+// copies.  Every barrier wait is bounded; on expiry the error word is set, work
+// stops, the accumulator is still committed (so no MMA is in flight at exit), copies
+// in flight are awaited (bounded) and TMEM is freed on every path.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "stream_args.h"
+
+namespace hsp {
+
+constexpr int kUmmaThreads = 128;
+constexpr uint32_t kWBoxBytes = 128u * 128u;  // 128 rows x 128 bytes
+
+template <int NT>
+struct UmmaCfg {
+    static_assert(NT == 16 || NT == 32 || NT == 64, "token tile");
+    static constexpr uint32_t kTmemCols = NT < 32 ? 32 : NT;
+};
+
+__device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns, volatile int *abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 7u) == 7u && ((*abort_flag != 0) || (global_timer_ns() - t0 > limit_ns))) return false;
+    }
+}
+
+template <int COMPUTE>
+__device__ __forceinline__ void umma_store(const UmmaArgs &a, int n, int tok, float v) {
+    int i = 0;
+#pragma unroll 1
+    while (i + 1 < a.splits.count && n >= a.splits.off[i + 1]) ++i;
+    const int64_t idx = static_cast<int64_t>(tok) * a.splits.rows[i] + (n - a.splits.off[i]);
+    if constexpr (COMPUTE == kMmaBf16)
+        static_cast<__nv_bfloat16 *>(a.splits.out[i])[idx] = __float2bfloat16_rn(v);
+    else
+        static_cast<float *>(a.splits.out[i])[idx] = v;
+}
+
+template <int COMPUTE, int NT>
+__global__ void __launch_bounds__(kUmmaThreads, 1)
+    hsp_umma_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                    const __grid_constant__ UmmaArgs a) {
+    using C = UmmaCfg<NT>;
+    constexpr int kBoxK = (COMPUTE == kMmaBf16) ? 64 : 32;  // elements per 128-byte k-block
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t ring_bytes = a.ring_stages * a.stage_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ring_bytes);
+    uint64_t *empty = full + a.ring_stages;
+    uint64_t *accf = empty + a.ring_stages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *issued = const_cast<int *>(abort_flag) + 1;  // k-blocks whose copies were issued
+    float *red = reinterpret_cast<float *>(smem);      // receive buffer of the cluster reduction
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row0 = blockIdx.x * 128;
+    const int rows_here = min(128, a.n_rows - row0);
+    const int slice = blockIdx.y;
+    const int kb0 = slice * a.kb_per_slice;
+    const int nkb = max(0, min(a.kb_total, kb0 + a.kb_per_slice) - kb0);
+
+    if (tid == 0) {
+        for (int s = 0; s < a.ring_stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(accf), 1);
+        *abort_flag = 0;
+        *issued = 0;
+        mbar_fence_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_d = *tmem_slot;
+
+    if (warp >= 2 && a.prefetch_l2 && nkb > 0) {
+        // One contiguous run per weight row: this slice's k-blocks of that row.
+        const int64_t b0 = static_cast<int64_t>(kb0) * 128;
+        const int64_t b1 = min(static_cast<int64_t>(kb0 + nkb) * 128, a.row_bytes);
+        const uint32_t nbytes = static_cast<uint32_t>(b1 - b0);
+        for (int r = (warp - 2) * 32 + lane; r < rows_here; r += 64)
+            bulk_prefetch_l2(a.w + (row0 + r) * a.row_bytes + b0, nbytes);
+    }
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- copy producer ----------------
+        tma_prefetch_map(&tmap_w);
+        tma_prefetch_map(&tmap_x);
+        const int npre = min(nkb, a.ring_stages);
+        for (int i = 0; i < npre; ++i) {
+            if (i == a.skip_stage) continue;
+            const uint32_t fb = smem_u32(&full[i]);
+            mbar_expect_tx(fb, kWBoxBytes);
+            tma_load_2d(ring + i * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb);
+        }
+        griddep_wait();
+        for (int i = 0; i < npre; ++i) {
+            if (i == a.skip_stage) continue;
+            const uint32_t fb = smem_u32(&full[i]);
+            mbar_arrive_expect_tx(fb, a.x_box_bytes);
+            tma_load_2d(ring + i * a.stage_bytes + kWBoxBytes, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
+            *issued = i + 1;
+        }
+        for (int i = npre; i < nkb; ++i) {
+            const int slot = i % a.ring_stages;
+            const uint32_t par = static_cast<uint32_t>((i / a.ring_stages) - 1) & 1u;
+            if (!umma_wait(smem_u32(&empty[slot]), par, a.wait_limit_ns, abort_flag)) {
+                atomicCAS(a.err_word, 0, kDeviceErrTimeout);
+                *abort_flag = 1;
+                break;
+            }
+            if (i == a.skip_stage) continue;
+            const uint32_t fb = smem_u32(&full[slot]);
+            mbar_arrive_expect_tx(fb, kWBoxBytes + a.x_box_bytes);
+            tma_load_2d(ring + slot * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb);
+            tma_load_2d(ring + slot * a.stage_bytes + kWBoxBytes, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
+            *issued = i + 1;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t kFmt = (COMPUTE == kMmaBf16) ? 1u : 2u;  // bf16 (kind::f16) / tf32 (kind::tf32)
+        const uint32_t idesc = (1u << 4)                       // D: f32
+                               | (kFmt << 7) | (kFmt << 10)    // A, B element type
+                               | (static_cast<uint32_t>(NT >> 3) << 17)  // N
+                               | (static_cast<uint32_t>(128 >> 4) << 24); // M
+        for (int i = 0; i < nkb; ++i) {
+            const int slot = i % a.ring_stages;
+            const uint32_t par = static_cast<uint32_t>(i / a.ring_stages) & 1u;
+            if (!umma_wait(smem_u32(&full[slot]), par, a.wait_limit_ns, abort_flag)) {
+                atomicCAS(a.err_word, 0, kDeviceErrTimeout);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t wa = ring + slot * a.stage_bytes;
+            const uint32_t xa = wa + kWBoxBytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = umma_desc_sw128(wa + k * 32);
+                const uint64_t bd = umma_desc_sw128(xa + k * 32);
+                if constexpr (COMPUTE == kMmaBf16)
+                    umma_f16(tmem_d, ad, bd, idesc, (i | k) != 0 ? 1u : 0u);
+                else
+                    umma_tf32(tmem_d, ad, bd, idesc, (i | k) != 0 ? 1u : 0u);
+            }
+            umma_commit(smem_u32(&empty[slot]));
+        }
+        // Always committed, so that no MMA is in flight when the accumulator is read
+        // or the tensor memory freed (also after a timeout).
+        umma_commit(smem_u32(accf));
+    }
+    __syncwarp();
+
+    // ---------------- epilogue ----------------
+    const bool acc_ok = umma_wait(smem_u32(accf), 0u, a.wait_limit_ns, abort_flag);
+    if (!acc_ok && lane == 0) {
+        atomicCAS(a.err_word, 0, kDeviceErrTimeout);
+        *abort_flag = 1;
+    }
+    tc_fence_after_sync();
+    __syncthreads();
+    const bool aborted = (*abort_flag != 0);
+    const bool have_acc = !aborted && nkb > 0;  // an empty K slice contributes zeros
+    if (*abort_flag != 0 && tid == 0) {
+        // copies still in flight land before the shared memory is reused or freed
+        const int n_iss = *issued;
+        for (int i = max(0, n_iss - a.ring_stages); i < n_iss; ++i) {
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(smem_u32(&full[i % a.ring_stages]), static_cast<uint32_t>(i / a.ring_stages) & 1u) &&
+                   global_timer_ns() - t0 < a.wait_limit_ns / 16 + 1) {
+            }
+        }
+    }
+    __syncthreads();
+
+    // thread (warp w, lane l) owns weight row 32w + l of the tile
+    const int r = warp * 32 + lane;
+    float v[NT];
+    if (have_acc) {
+#pragma unroll
+        for (int c = 0; c < NT; c += 16) {
+            float t[16];
+            tmem_ld16(tmem_d + (static_cast<uint32_t>(warp * 32) << 16) + c, t);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[c + q] = t[q];
+        }
+        tmem_wait_ld();
+    } else {
+#pragma unroll
+        for (int c = 0; c < NT; ++c) v[c] = 0.f;
+    }
+    tc_fence_before_sync();
+
+    griddep_wait();  // outputs may still be read by the previous kernel on the stream
+    bool stored = false;
+    if (a.slices == 1) {
+        if (!aborted && r < rows_here) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                if (t < a.M) umma_store<COMPUTE>(a, row0 + r, t, v[t]);
+            stored = true;
+        }
+    } else {
+        // Push model: every CTA writes its partial rows into the receive buffer of the
+        // CTA that owns them (remote stores do not wait), then each owner adds the S
+        // slices of its rows in slice order from local shared memory.
+        // recv[q][row][token] with a row pitch of NT + 4 floats (16-byte aligned, fewer
+        // bank conflicts); it aliases the ring, which every CTA has left once the
+        // first cluster barrier is passed.
+        constexpr int kPitch = NT + 4;
+        const int per = 128 / a.slices;
+        const uint32_t recv_local = smem_u32(red);
+        cluster_sync_all();
+        {
+            const int q = r / per, rr = r - q * per;
+            const uint32_t dst = cluster_map_shared(
+                recv_local + static_cast<uint32_t>(((slice * per + rr) * kPitch) * 4), static_cast<uint32_t>(q));
+#pragma unroll
+            for (int c = 0; c < NT; c += 4) st_shared_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
+        }
+        cluster_sync_all();
+        if (!aborted) {
+            constexpr int kT4 = NT / 4;
+            for (int e = tid; e < per * kT4; e += kUmmaThreads) {
+                const int rr = e / kT4, t4 = (e - rr * kT4) * 4;
+                const int row = slice * per + rr;
+                if (row >= rows_here || t4 >= a.M) continue;
+                float4 part[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < a.slices) part[q] = *reinterpret_cast<const float4 *>(red + (q * per + rr) * kPitch + t4);
+                float4 acc = part[0];
+#pragma unroll
+                for (int q = 1; q < 8; ++q)
+                    if (q < a.slices) {
+                        acc.x += part[q].x;
+                        acc.y += part[q].y;
+                        acc.z += part[q].z;
+                        acc.w += part[q].w;
+                    }
+                const float o[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (t4 + j < a.M) umma_store<COMPUTE>(a, row0 + row, t4 + j, o[j]);
+                stored = true;
+            }
+        }
+    }
+    if (stored) fence_release_gpu();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_d, C::kTmemCols);
+    }
+    griddep_launch_dependents();
+}
+
+}  // namespace hsp

@@ -82,13 +82,21 @@ typedef struct {
      * to test the timeout path.  Never faults: nothing is read or written out of
      * bounds and every wait is bounded. */
     int32_t skip_stage_plus1;
-    int32_t reserved[5];
+    /* Kernel for bf16 with 9 <= M <= 64: 0 (default) = tensor-memory kernel
+     * (tcgen05.mma into TMEM, tensor copies of the operands); 1 = the bulk-copy
+     * mma.sync kernel that also serves M <= 8, tf32 and fp32.  Both give results within
+     * tolerance; each is bitwise self-consistent (fused = separate, run to run). */
+    int32_t large_m_path;
+    /* 1: the tensor-memory kernel first prefetches each CTA's weight rows into L2 as
+     * contiguous runs.  0 (default): no prefetch (measured slower on GB300). */
+    int32_t l2_prefetch;
+    int32_t reserved[3];
 } proj_options;
 
 /* Kernel geometry chosen for one launch (proj_describe_plan). */
 typedef struct {
     int32_t bucket;        /* 0: M <= 8, 1: 9 <= M <= 32, 2: 33 <= M <= 64 */
-    int32_t compute;       /* 0 bf16 mma.sync, 1 tf32 mma.sync, 2 fp32 FMA */
+    int32_t compute;       /* 0 bf16 tensor cores, 1 tf32 tensor cores, 2 fp32 FMA */
     int32_t rows_per_cta;  /* R: output rows owned by one CTA */
     int32_t row_ctas;      /* CTAs along the rows (grid.x) */
     int32_t slices;        /* S: K slices = CTAs per cluster (grid.y) */
@@ -103,7 +111,8 @@ typedef struct {
     int32_t stages_total;  /* ring stages of one K slice */
     int32_t threads;       /* threads per CTA (consumer warps + 1 producer warp) */
     int32_t units_per_slice; /* 128-byte k-units per K slice (fixes the summation order with k_warps) */
-    int32_t reserved[4];
+    int32_t engine;          /* 0 bulk-copy + mma.sync / FMA kernel, 1 tensor-memory (tcgen05) kernel */
+    int32_t reserved[3];
 } proj_plan_info;
 
 /*

@@ -112,12 +112,18 @@ def test_plan_fits_the_hardware(hsp):
                 for n in (wl.n_total, *wl.splits):
                     p = hsp.describe_plan(M, wl.K, n, dt)
                     assert p["smem_bytes"] <= 232448
-                    assert p["rows_per_cta"] <= p["row_warps"] * p["row_tiles"] * 16
-                    assert p["rows_per_cta"] <= 256
-                    assert p["ring_stages"] >= 1
-                    assert (p["row_warps"] * p["row_tiles"] * 16) % p["slices"] == 0
                     assert p["row_ctas"] * p["rows_per_cta"] >= n
-                    assert p["threads"] == 288
+                    assert p["slices"] in (1, 2, 4, 8)
+                    if p["engine"] == 0:     # bulk-copy + mma.sync / FMA kernel
+                        assert p["rows_per_cta"] <= p["row_warps"] * p["row_tiles"] * 16
+                        assert p["ring_stages"] >= 1
+                        assert (p["row_warps"] * p["row_tiles"] * 16) % p["slices"] == 0
+                        assert p["threads"] == 288
+                    else:                    # tensor-memory kernel: 128-row tiles, 2 CTAs per SM
+                        assert M > 8 and dt == 0
+                        assert p["rows_per_cta"] == 128 and p["threads"] == 128
+                        assert p["smem_bytes"] <= 113 * 1024
+                        assert p["ring_stages"] >= 2 and 128 % p["slices"] == 0
 
 
 def test_pack_check_and_options(hsp):
@@ -128,8 +134,12 @@ def test_pack_check_and_options(hsp):
     assert lib.proj_pack_check(base + 1280 * K * 2 + 2, base, 1280, 512, 1792, K, 0) == 0
     assert lib.proj_pack_check(base, base, 1280, 513, 1792, K, 0) == 0
     hsp.set_options(pdl=False, wait_limit_us=5, skip_stage=3)
-    assert hsp.get_options() == {"pdl": 0, "wait_limit_us": 5, "skip_stage_plus1": 4}
+    assert hsp.get_options() == {"pdl": 0, "wait_limit_us": 5, "skip_stage_plus1": 4,
+                                 "large_m_path": 0, "l2_prefetch": 0}
+    hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None, large_m_path=1, l2_prefetch=True)
+    assert hsp.get_options()["large_m_path"] == 1 and hsp.get_options()["l2_prefetch"] == 1
     hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None)
-    assert hsp.get_options() == {"pdl": 1, "wait_limit_us": 0, "skip_stage_plus1": 0}
+    assert hsp.get_options() == {"pdl": 1, "wait_limit_us": 0, "skip_stage_plus1": 0,
+                                 "large_m_path": 0, "l2_prefetch": 0}
     with pytest.raises(hsp.ProjError):
         hsp.set_options(wait_limit_us=-1)
