@@ -349,6 +349,9 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, UPlan *p) {
     int ring = (110 * 1024) / p->stage_bytes;
     if (ring < 2) ring = 2;
     if (ring > p->kb_per_slice) ring = p->kb_per_slice < 2 ? 2 : p->kb_per_slice;
+    // the ring also holds the cluster reduction's staging and receive buffers
+    const int reduce_bytes = 2 * 128 * (p->NT + 4) * 4;
+    while (p->S > 1 && ring * p->stage_bytes < reduce_bytes) ++ring;
     p->ring = ring;
     p->smem = 1024 + ring * p->stage_bytes + (2 * ring + 1) * 8 + 16 + 64;
     proj_plan_info &i = p->info;

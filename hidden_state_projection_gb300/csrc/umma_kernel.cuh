@@ -17,9 +17,9 @@
 //     K = 16 bf16 or 8 tf32 each) per k-block into one TMEM accumulator and commits
 //     each stage back to the ring; a final commit marks the accumulator ready;
 //   * all four warps read the accumulator (warp w owns TMEM lanes 32w..32w+31, one
-//     weight row per thread), then either store (S = 1) or push each row's partial
-//     into the shared memory of the CTA that owns the row (st.shared::cluster), and
-//     the owner adds the S slices in slice order and stores.  The sum of every
+//     weight row per thread), then either store (S = 1) or push the partials of
+//     each owner's rows into that CTA's shared memory (coalesced st.shared::cluster),
+//     and the owner adds the S slices in slice order and stores.  The sum of every
 //     output is the tensor-core accumulation over K in order, then slices in order:
 //     a function of (K, dtype, M bucket) only, never of the row's place in a tile.
 //   * the trigger follows a release fence in every storing thread (TensorRT-LLM PR
@@ -242,34 +242,48 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             stored = true;
         }
     } else {
-        // Push model: every CTA writes its partial rows into the receive buffer of the
-        // CTA that owns them (remote stores do not wait), then each owner adds the S
-        // slices of its rows in slice order from local shared memory.
-        // recv[q][row][token] with a row pitch of NT + 4 floats (16-byte aligned, fewer
-        // bank conflicts); it aliases the ring, which every CTA has left once the
-        // first cluster barrier is passed.
+        // Push model.  Each thread first puts its row's partial into a local staging
+        // buffer laid out as one contiguous block per owner CTA, [owner][row][token]
+        // with a row pitch of NT + 4 floats; after the first cluster barrier (every CTA
+        // has left its ring, which both buffers alias) the CTA copies block q into the
+        // receive buffer of CTA q with coalesced remote stores (consecutive lanes,
+        // consecutive 16 bytes; remote stores do not wait).  After the second barrier
+        // each owner adds the S slices of its rows in slice order from local memory.
         constexpr int kPitch = NT + 4;
         const int per = 128 / a.slices;
-        const uint32_t recv_local = smem_u32(red);
-        cluster_sync_all();
+        const int block = per * kPitch;                 // floats per owner block
+        float *staging = red;
+        float *recv = red + 128 * kPitch;
         {
             const int q = r / per, rr = r - q * per;
-            const uint32_t dst = cluster_map_shared(
-                recv_local + static_cast<uint32_t>(((slice * per + rr) * kPitch) * 4), static_cast<uint32_t>(q));
+            float *dst = staging + q * block + rr * kPitch;
 #pragma unroll
-            for (int c = 0; c < NT; c += 4) st_shared_cluster_v4(dst + c * 4, v[c], v[c + 1], v[c + 2], v[c + 3]);
+            for (int c = 0; c < NT; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+        }
+        __syncthreads();
+        cluster_sync_all();
+        {
+            const uint32_t recv_local = smem_u32(recv);
+            const int chunks = block / 4;               // 16-byte chunks per owner block
+            for (int c = tid; c < a.slices * chunks; c += kUmmaThreads) {
+                const int q = c / chunks, off = c - q * chunks;
+                const float4 val = *reinterpret_cast<const float4 *>(staging + q * block + off * 4);
+                const uint32_t dst = recv_local + static_cast<uint32_t>((slice * block + off * 4) * 4);
+                st_shared_cluster_v4(cluster_map_shared(dst, static_cast<uint32_t>(q)), val.x, val.y, val.z, val.w);
+            }
         }
         cluster_sync_all();
         if (!aborted) {
             constexpr int kT4 = NT / 4;
+            // consecutive threads take consecutive rows of the same four tokens
             for (int e = tid; e < per * kT4; e += kUmmaThreads) {
-                const int rr = e / kT4, t4 = (e - rr * kT4) * 4;
+                const int t4 = (e / per) * 4, rr = e - (e / per) * per;
                 const int row = slice * per + rr;
                 if (row >= rows_here || t4 >= a.M) continue;
                 float4 part[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    if (q < a.slices) part[q] = *reinterpret_cast<const float4 *>(red + (q * per + rr) * kPitch + t4);
+                    if (q < a.slices) part[q] = *reinterpret_cast<const float4 *>(recv + q * block + rr * kPitch + t4);
                 float4 acc = part[0];
 #pragma unroll
                 for (int q = 1; q < 8; ++q)
