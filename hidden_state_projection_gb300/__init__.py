@@ -30,7 +30,7 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 MAX_SPLITS = 8
 MAX_M = 64
 
-EXPORTED = ("proj_fused_gemm", "proj_separate_gemm", "proj_pack_weights", "proj_pack_check",
+EXPORTED = ("proj_fused_gemm", "proj_fused_gemm_prefetch", "proj_separate_gemm", "proj_pack_weights", "proj_pack_check",
             "proj_supported", "proj_describe_plan", "proj_set_options", "proj_get_options",
             "proj_check_device_error", "proj_launch_count", "proj_last_error_string", "proj_version")
 
@@ -46,6 +46,10 @@ class Options(ctypes.Structure):
     _fields_ = [("pdl", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
                 ("skip_stage_plus1", ctypes.c_int32), ("large_m_path", ctypes.c_int32),
                 ("l2_prefetch", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+
+class PrefetchRange(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("bytes", ctypes.c_uint64)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -75,6 +79,8 @@ def lib() -> ctypes.CDLL:
     for name in ("proj_fused_gemm", "proj_separate_gemm"):
         getattr(L, name).argtypes = gemm_args
         getattr(L, name).restype = ctypes.c_int
+    L.proj_fused_gemm_prefetch.argtypes = gemm_args[:8] + [ctypes.POINTER(PrefetchRange), i32, vp]
+    L.proj_fused_gemm_prefetch.restype = ctypes.c_int
     L.proj_pack_weights.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, ctypes.c_int, vp, vp]
     L.proj_pack_weights.restype = ctypes.c_int
     L.proj_pack_check.argtypes = [vp, vp, i64, i32, i32, i32, ctypes.c_int]
@@ -130,6 +136,15 @@ def fused_gemm_ptr(x_ptr: int, w_ptr: int, splits: Sequence[int], out_ptrs: Sequ
     _check(lib().proj_fused_gemm(x_ptr, w_ptr, ns, len(splits), po, M, K, dtype, stream_ptr))
 
 
+def fused_gemm_prefetch_ptr(x_ptr: int, w_ptr: int, splits: Sequence[int], out_ptrs: Sequence[int],
+                            M: int, K: int, dtype: int, prefetch: Sequence[tuple], stream_ptr: int = 0) -> None:
+    ns = (ctypes.c_int32 * len(splits))(*[int(s) for s in splits])
+    po = (ctypes.c_void_p * len(out_ptrs))(*[int(p) for p in out_ptrs])
+    pr = (PrefetchRange * max(1, len(prefetch)))(*[PrefetchRange(int(p), int(b)) for p, b in prefetch])
+    _check(lib().proj_fused_gemm_prefetch(x_ptr, w_ptr, ns, len(splits), po, M, K, dtype, pr, len(prefetch),
+                                          stream_ptr))
+
+
 def separate_gemm_ptr(x_ptr: int, w_ptr: int, splits: Sequence[int], out_ptrs: Sequence[int],
                       M: int, K: int, dtype: int, stream_ptr: int = 0) -> None:
     ns = (ctypes.c_int32 * len(splits))(*[int(s) for s in splits])
@@ -168,6 +183,17 @@ def fused_gemm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
                outs: Optional[List[torch.Tensor]] = None, tf32: bool = False, stream=None):
     """One launch over all of w_cat; returns one dense [M, N_i] tensor per split."""
     return _gemm(fused_gemm_ptr, x, w_cat, splits, outs, tf32, stream)
+
+
+def fused_gemm_prefetch(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
+                        prefetch: Sequence[torch.Tensor], outs: Optional[List[torch.Tensor]] = None,
+                        tf32: bool = False, stream=None):
+    """fused_gemm that also prefetches the given tensors (e.g. the next layer's weights) into L2."""
+    ranges = [(t.data_ptr(), t.numel() * t.element_size()) for t in prefetch]
+
+    def fn(xp, wp, sp, op, M, K, dt, st):
+        fused_gemm_prefetch_ptr(xp, wp, sp, op, M, K, dt, ranges, st)
+    return _gemm(fn, x, w_cat, splits, outs, tf32, stream)
 
 
 def separate_gemm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],

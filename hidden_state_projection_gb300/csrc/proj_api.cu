@@ -375,7 +375,8 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, UPlan *p) {
 }
 
 proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
-                             proj_dtype dt, const hsp::SplitTable &splits, cudaStream_t stream) {
+                             proj_dtype dt, const hsp::SplitTable &splits, const hsp::PrefetchList &pf,
+                             cudaStream_t stream) {
     UPlan p;
     make_umma_plan(M, K, n_rows, dt, &p);
     hsp::UmmaLaunchReq r{};
@@ -408,6 +409,7 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
     a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
     a.err_word = dev.err_word;
     a.splits = splits;
+    a.prefetch = pf;
     cudaError_t e = hsp::launch_umma(r);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch (tensor-memory path)");
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -416,8 +418,9 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
 
 // One launch over `n_rows` weight rows starting at `w` (already offset to the first row).
 proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
-                        proj_dtype dt, const hsp::SplitTable &splits, cudaStream_t stream) {
-    if (use_umma(M, dt)) return launch_umma_rows(dev, x, w, n_rows, M, K, dt, splits, stream);
+                        proj_dtype dt, const hsp::SplitTable &splits, const hsp::PrefetchList &pf,
+                        cudaStream_t stream) {
+    if (use_umma(M, dt)) return launch_umma_rows(dev, x, w, n_rows, M, K, dt, splits, pf, stream);
     Plan p;
     make_plan(M, K, n_rows, dt, dev.cluster_ctas, &p);
     if (p.ring_stages < 1 || p.smem > kSmemLimit)
@@ -452,6 +455,7 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
     a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
     a.err_word = dev.err_word;
     a.splits = splits;
+    a.prefetch = pf;
     cudaError_t e = cudaSuccess;
     switch (p.compute) {
         case hsp::kMmaBf16: e = hsp::launch_bf16(r); break;
@@ -492,12 +496,9 @@ proj_status validate(const void *x, const void *w_cat, const int32_t *n_splits, 
     return PROJ_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
-                            void *const *outs, int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream) {
+proj_status fused_impl(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                       void *const *outs, int32_t M, int32_t K, proj_dtype dtype, const hsp::PrefetchList &pf,
+                       proj_stream_t stream) {
     int64_t n_total = 0;
     proj_status st = validate(x, w_cat, n_splits, num_splits, outs, M, K, dtype, &n_total);
     if (st != PROJ_OK) return st;
@@ -514,8 +515,38 @@ proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_s
         t.out[i] = outs[i];
         off += n_splits[i];
     }
-    st = launch_rows(dev, x, w_cat, static_cast<int>(n_total), M, K, dtype, t, reinterpret_cast<cudaStream_t>(stream));
+    st = launch_rows(dev, x, w_cat, static_cast<int>(n_total), M, K, dtype, t, pf,
+                     reinterpret_cast<cudaStream_t>(stream));
     return st == PROJ_OK ? ok() : st;
+}
+
+}  // namespace
+
+extern "C" {
+
+proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                            void *const *outs, int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream) {
+    hsp::PrefetchList none;
+    memset(&none, 0, sizeof none);
+    return fused_impl(x, w_cat, n_splits, num_splits, outs, M, K, dtype, none, stream);
+}
+
+proj_status proj_fused_gemm_prefetch(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                                     void *const *outs, int32_t M, int32_t K, proj_dtype dtype,
+                                     const proj_prefetch_range *ranges, int32_t num_ranges, proj_stream_t stream) {
+    if (num_ranges < 0 || num_ranges > PROJ_MAX_PREFETCH || (num_ranges > 0 && !ranges))
+        return fail(PROJ_ERR_INVALID_ARG, "num_ranges=%d (0..%d) or ranges NULL", num_ranges, PROJ_MAX_PREFETCH);
+    hsp::PrefetchList pf;
+    memset(&pf, 0, sizeof pf);
+    for (int i = 0; i < num_ranges; ++i) {
+        if (!ranges[i].ptr || ranges[i].bytes == 0) return fail(PROJ_ERR_INVALID_ARG, "prefetch range %d is empty", i);
+        if (!aligned16(ranges[i].ptr) || ranges[i].bytes % 16 != 0)
+            return fail(PROJ_ERR_MISALIGNED, "prefetch range %d: pointer and size must be multiples of 16 bytes", i);
+        pf.ptr[pf.count] = static_cast<const char *>(ranges[i].ptr);
+        pf.bytes[pf.count] = ranges[i].bytes;
+        ++pf.count;
+    }
+    return fused_impl(x, w_cat, n_splits, num_splits, outs, M, K, dtype, pf, stream);
 }
 
 proj_status proj_separate_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
@@ -535,7 +566,9 @@ proj_status proj_separate_gemm(const void *x, const void *w_cat, const int32_t *
         t.rows[0] = n_splits[i];
         t.out[0] = outs[i];
         const void *wi = static_cast<const char *>(w_cat) + off * pitch;
-        st = launch_rows(dev, x, wi, n_splits[i], M, K, dtype, t, reinterpret_cast<cudaStream_t>(stream));
+        hsp::PrefetchList none;
+        memset(&none, 0, sizeof none);
+        st = launch_rows(dev, x, wi, n_splits[i], M, K, dtype, t, none, reinterpret_cast<cudaStream_t>(stream));
         if (st != PROJ_OK) return st;
         off += static_cast<size_t>(n_splits[i]);
     }

@@ -10,6 +10,16 @@ enum Compute : int { kMmaBf16 = 0, kMmaTf32 = 1, kFmaFp32 = 2 };
 constexpr int kMaxSplits = 8;
 constexpr int kDeviceErrTimeout = 7;  // same value as PROJ_ERR_TIMEOUT
 constexpr int kUnitBytes = 128;       // one k-unit: 128 bytes of a row (64 bf16 or 32 fp32)
+constexpr int kMaxPrefetch = 4;       // caller tensors prefetched into L2 by one call
+constexpr uint32_t kPrefetchChunk = 16384;
+
+// Global ranges a call prefetches into L2 for later kernels (16-byte aligned,
+// sizes multiples of 16), cut into 16 KB chunks spread over the CTAs.
+struct PrefetchList {
+    int32_t count;
+    const char *ptr[kMaxPrefetch];
+    uint64_t bytes[kMaxPrefetch];
+};
 
 // Output scatter: row n of the launch (0-based in its weight rows) belongs to
 // split i with off[i] <= n < off[i] + rows[i]; element (token t, row n) goes to
@@ -47,6 +57,7 @@ struct StreamArgs {
     uint64_t wait_limit_ns;    // bound of every barrier wait
     int *err_word;             // device error word (PROJ_ERR_TIMEOUT on expiry)
     SplitTable splits;
+    PrefetchList prefetch;
 };
 
 // Tensor-memory path (9 <= M <= 64): a CTA owns a 128-row weight tile and one
@@ -68,6 +79,7 @@ struct UmmaArgs {
     uint64_t wait_limit_ns;
     int *err_word;
     SplitTable splits;
+    PrefetchList prefetch;
 };
 
 }  // namespace hsp

@@ -50,6 +50,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "prefetch.cuh"
 #include "ptx.cuh"
 #include "stream_args.h"
 
@@ -342,6 +343,9 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         __syncwarp();
         issue_w(i, b0, nb, smem_u32(&full[i]));
     }
+    // Weights of later kernels named by the caller: into L2, before the grid dependency.
+    if (warp == C::kNCW && a.prefetch.count > 0)
+        prefetch_ranges_l2(a.prefetch, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y, lane);
     // Activations are written by the previous kernel on the stream.
     griddep_wait();
     for (int i = 0; i < npre; ++i) {

@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "prefetch.cuh"
 #include "ptx.cuh"
 #include "stream_args.h"
 
@@ -122,6 +123,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         for (int r = (warp - 2) * 32 + lane; r < rows_here; r += 64)
             bulk_prefetch_l2(a.w + (row0 + r) * a.row_bytes + b0, nbytes);
     }
+
+    // Weights of later kernels named by the caller: into L2, before the grid dependency.
+    if (warp == 3 && a.prefetch.count > 0)
+        prefetch_ranges_l2(a.prefetch, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y, lane);
 
     if (warp == 0 && lane == 0) {
         // ---------------- copy producer ----------------

@@ -63,6 +63,13 @@ typedef enum {
 
 #define PROJ_MAX_SPLITS 8
 #define PROJ_MAX_M 64
+#define PROJ_MAX_PREFETCH 4
+
+/* A global range to bring into L2 (proj_fused_gemm_prefetch). */
+typedef struct {
+    const void *ptr;  /* device pointer, 16-byte aligned */
+    uint64_t bytes;   /* a multiple of 16 */
+} proj_prefetch_range;
 
 /* Process-wide options (proj_set_options).  Zero-initialised = defaults. */
 typedef struct {
@@ -133,6 +140,20 @@ typedef struct {
 proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_splits,
                             int32_t num_splits, void *const *outs, int32_t M, int32_t K,
                             proj_dtype dtype, proj_stream_t stream);
+
+/*
+ * proj_fused_gemm_prefetch -- proj_fused_gemm that also prefetches up to
+ * PROJ_MAX_PREFETCH caller-named global ranges into L2 (TensorRT-LLM PR #20502,
+ * glmFusedAGemm commit message: before the grid-dependency wait each CTA prefetches
+ * up to four caller tensors -- weights that later kernels of the step read -- into
+ * L2 in 16 KB bulk prefetches spread over the CTAs).  The ranges are only read as
+ * a hint: the outputs are bitwise those of proj_fused_gemm.  Ranges must stay
+ * allocated until the call has completed on the stream.
+ */
+proj_status proj_fused_gemm_prefetch(const void *x, const void *w_cat, const int32_t *n_splits,
+                                     int32_t num_splits, void *const *outs, int32_t M, int32_t K,
+                                     proj_dtype dtype, const proj_prefetch_range *ranges,
+                                     int32_t num_ranges, proj_stream_t stream);
 
 /*
  * proj_separate_gemm -- one launch per projection over its row range of the same

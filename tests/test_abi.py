@@ -143,3 +143,19 @@ def test_pack_check_and_options(hsp):
                                  "large_m_path": 0, "l2_prefetch": 0}
     with pytest.raises(hsp.ProjError):
         hsp.set_options(wait_limit_us=-1)
+
+
+def test_prefetch_entry_validation(hsp):
+    import ctypes
+    S = hsp.STATUS
+    lib = hsp.lib()
+    ns = (ctypes.c_int32 * 2)(16, 8)
+    po = (ctypes.c_void_p * 2)(0x30000, 0x31000)
+    def call(ranges, n):
+        arr = (hsp.PrefetchRange * max(1, len(ranges)))(*[hsp.PrefetchRange(p, b) for p, b in ranges])
+        return lib.proj_fused_gemm_prefetch(0x10000, 0x20000, ns, 2, po, 1, 64, 0, arr, n, None)
+    assert call([], 5) == S["PROJ_ERR_INVALID_ARG"]
+    assert call([(0, 64)], 1) == S["PROJ_ERR_INVALID_ARG"]
+    assert call([(0x40008, 64)], 1) == S["PROJ_ERR_MISALIGNED"]
+    assert call([(0x40000, 60)], 1) == S["PROJ_ERR_MISALIGNED"]
+    assert call([(0x40000, 0)], 1) == S["PROJ_ERR_INVALID_ARG"]

@@ -110,3 +110,13 @@ def test_bounded_wait_reports_timeout(hsp, name, M):
     again = hsp.fused_gemm(x, w, wl.splits)
     hsp.check_device_error()
     assert all(torch.equal(a, b) for a, b in zip(good, again))
+
+
+@pytest.mark.parametrize("name,M,tf32", CFGS)
+def test_prefetch_variant_is_bitwise_equal(hsp, name, M, tf32):
+    wl, x, w = _inputs(name, M, 3)
+    other = W.weight_cat(wl, 1).cuda()
+    a = hsp.fused_gemm(x, w, wl.splits, tf32=tf32)
+    b = hsp.fused_gemm_prefetch(x, w, wl.splits, [other, x], tf32=tf32)
+    hsp.check_device_error()
+    assert all(torch.equal(p, q) for p, q in zip(a, b))

@@ -135,3 +135,20 @@ def test_empty_batch_is_a_no_op(hsp):
     outs = hsp.fused_gemm(x, w, splits)
     assert [tuple(o.shape) for o in outs] == [(0, 16), (0, 8)]
     assert hsp.launch_count() == before
+
+
+@pytest.mark.parametrize("M", [9, 16, 17, 32, 33, 64])
+def test_large_m_streaming_engine_matches_oracle(hsp, M):
+    """bf16 at M > 8 normally runs the tensor-memory kernel; the bulk-copy mma.sync
+    kernel stays selectable and must agree with the oracle too."""
+    K, splits = 7168, (1536, 576, 128, 64)
+    x, ws = W.random_case(K, splits, M, "bf16", seed=900 + M)
+    w_cat = torch.cat(ws, 0)
+    hsp.set_options(pdl=True, large_m_path=1)
+    try:
+        assert hsp.describe_plan(M, K, sum(splits), 0)["engine"] == 0
+        outs = _run_both(hsp, x, w_cat, splits)
+    finally:
+        hsp.set_options(pdl=True, large_m_path=0)
+    assert hsp.describe_plan(M, K, sum(splits), 0)["engine"] == 1
+    check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"stream M{M}")
