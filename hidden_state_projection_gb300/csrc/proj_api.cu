@@ -43,6 +43,7 @@ std::atomic<int> g_opt_wait_us{0};
 std::atomic<int> g_opt_skip_stage_plus1{0};
 std::atomic<int> g_opt_large_m_path{0};
 std::atomic<int> g_opt_l2_prefetch{0};
+std::atomic<int> g_opt_trigger_early{0};
 
 }  // namespace
 
@@ -404,6 +405,7 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
     a.stage_bytes = static_cast<uint32_t>(p.stage_bytes);
     a.x_box_bytes = static_cast<uint32_t>(p.x_box);
     a.prefetch_l2 = g_opt_l2_prefetch.load();
+    a.trigger_early = g_opt_trigger_early.load();
     a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
     const int wus = g_opt_wait_us.load();
     a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
@@ -451,6 +453,7 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
     a.stage_bytes = static_cast<uint32_t>(p.stage_bytes);
     a.ring_bytes = static_cast<uint32_t>(p.ring_bytes);
     a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
+    a.trigger_early = g_opt_trigger_early.load();
     const int wus = g_opt_wait_us.load();
     a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
     a.err_word = dev.err_word;
@@ -647,13 +650,15 @@ proj_status proj_set_options(const proj_options *opt) {
     if (opt->pdl < -1 || opt->pdl > 1) return fail(PROJ_ERR_INVALID_ARG, "pdl must be -1, 0 or 1");
     if (opt->wait_limit_us < 0 || opt->skip_stage_plus1 < 0)
         return fail(PROJ_ERR_INVALID_ARG, "wait_limit_us and skip_stage_plus1 must be >= 0");
-    if (opt->large_m_path < 0 || opt->large_m_path > 1 || opt->l2_prefetch < 0 || opt->l2_prefetch > 1)
-        return fail(PROJ_ERR_INVALID_ARG, "large_m_path and l2_prefetch must be 0 or 1");
+    if (opt->large_m_path < 0 || opt->large_m_path > 1 || opt->l2_prefetch < 0 || opt->l2_prefetch > 1 ||
+        opt->trigger_early < 0 || opt->trigger_early > 1)
+        return fail(PROJ_ERR_INVALID_ARG, "large_m_path, l2_prefetch and trigger_early must be 0 or 1");
     if (opt->pdl >= 0) g_opt_pdl.store(opt->pdl);
     g_opt_wait_us.store(opt->wait_limit_us);
     g_opt_skip_stage_plus1.store(opt->skip_stage_plus1);
     g_opt_large_m_path.store(opt->large_m_path);
     g_opt_l2_prefetch.store(opt->l2_prefetch);
+    g_opt_trigger_early.store(opt->trigger_early);
     return ok();
 }
 
@@ -665,6 +670,7 @@ proj_status proj_get_options(proj_options *opt) {
     opt->skip_stage_plus1 = g_opt_skip_stage_plus1.load();
     opt->large_m_path = g_opt_large_m_path.load();
     opt->l2_prefetch = g_opt_l2_prefetch.load();
+    opt->trigger_early = g_opt_trigger_early.load();
     return ok();
 }
 

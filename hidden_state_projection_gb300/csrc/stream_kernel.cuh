@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         mbar_fence_init();
     }
     __syncthreads();
+    if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
 
     constexpr int kChains = (COMPUTE != kFmaFp32 && MT == 1) ? 2 : 1;
     float acc_mma[kChains][(COMPUTE == kFmaFp32) ? 1 : RT][(COMPUTE == kFmaFp32) ? 1 : MT][4];

@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_d = *tmem_slot;
+    if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
 
     if (warp >= 2 && a.prefetch_l2 && nkb > 0) {
         // One contiguous run per weight row: this slice's k-blocks of that row.

@@ -97,7 +97,12 @@ typedef struct {
     /* 1: the tensor-memory kernel first prefetches each CTA's weight rows into L2 as
      * contiguous runs.  0 (default): no prefetch (measured slower on GB300). */
     int32_t l2_prefetch;
-    int32_t reserved[3];
+    /* Test hook, 0 = off.  1: trigger the dependent launch at kernel start, before any
+     * output store (the order TensorRT-LLM PR #20636, Description, describes for
+     * tinygemm2).  Safe only for consumers that call griddepcontrol.wait; used by the
+     * PDL ordering test as its positive control. */
+    int32_t trigger_early;
+    int32_t reserved[2];
 } proj_options;
 
 /* Kernel geometry chosen for one launch (proj_describe_plan). */
