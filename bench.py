@@ -64,9 +64,11 @@ def kernel_sources_sha16():
 def profiled_traffic(name, M):
     """DRAM bytes per launch from the committed ncu summary of this workload, if that
     summary was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"hsp_stream_kernel_{name}_m{M}.md")
-    if not os.path.exists(path):
+    import glob
+    paths = glob.glob(os.path.join(ROOT, "profiles", f"hsp_*_kernel_{name}_m{M}.md"))
+    if not paths:
         return None
+    path = paths[0]
     fields = {}
     with open(path) as f:
         for line in f:
