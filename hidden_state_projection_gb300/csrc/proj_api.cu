@@ -44,6 +44,7 @@ std::atomic<int> g_opt_skip_stage_plus1{0};
 std::atomic<int> g_opt_large_m_path{0};
 std::atomic<int> g_opt_l2_prefetch{0};
 std::atomic<int> g_opt_trigger_early{0};
+std::atomic<int> g_opt_small_m_path{0};
 
 }  // namespace
 
@@ -181,6 +182,9 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     memset(p, 0, sizeof *p);
     const int esz = elem_size(dt);
     p->compute = dt == PROJ_BF16 ? hsp::kMmaBf16 : (dt == PROJ_TF32 ? hsp::kMmaTf32 : hsp::kFmaFp32);
+    // Opt-in for one or two tokens: fp32 FMA on the CUDA cores instead of an
+    // 8-token-wide mma.sync (measured slower on GB300: 8.4 vs 6.4 us for wq_a++wkv M=1).
+    if (dt == PROJ_BF16 && M <= 2 && g_opt_small_m_path.load() == 1) p->compute = hsp::kFmaBf16;
     p->bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
     static const int WRs[3] = {1, 2, 4}, WKs[3] = {8, 4, 2};
     p->WR = WRs[p->bucket];
@@ -195,6 +199,10 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     if (p->bucket > 0) {
         if (per_warp >= 16) p->S = 4;
         else if (per_warp >= 4) p->S = 2;
+    } else if (esz == 4 && per_warp >= 16) {
+        // fp32 rows are twice as long: few rows per CTA would leave most SMs idle and
+        // long per-warp chains; four K slices per row instead (fixed per K and dtype)
+        p->S = 4;
     }
     p->units_per_slice = ceil_div(ceil_div(p->units_total, p->S), p->WK) * p->WK;
     while (p->S > 1 && (p->S - 1) * p->units_per_slice >= p->units_total) {  // no empty slice
@@ -461,7 +469,8 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
     a.prefetch = pf;
     cudaError_t e = cudaSuccess;
     switch (p.compute) {
-        case hsp::kMmaBf16: e = hsp::launch_bf16(r); break;
+        case hsp::kMmaBf16:
+        case hsp::kFmaBf16: e = hsp::launch_bf16(r); break;
         case hsp::kMmaTf32: e = hsp::launch_tf32(r); break;
         default: e = hsp::launch_fp32(r); break;
     }
@@ -651,14 +660,15 @@ proj_status proj_set_options(const proj_options *opt) {
     if (opt->wait_limit_us < 0 || opt->skip_stage_plus1 < 0)
         return fail(PROJ_ERR_INVALID_ARG, "wait_limit_us and skip_stage_plus1 must be >= 0");
     if (opt->large_m_path < 0 || opt->large_m_path > 1 || opt->l2_prefetch < 0 || opt->l2_prefetch > 1 ||
-        opt->trigger_early < 0 || opt->trigger_early > 1)
-        return fail(PROJ_ERR_INVALID_ARG, "large_m_path, l2_prefetch and trigger_early must be 0 or 1");
+        opt->trigger_early < 0 || opt->trigger_early > 1 || opt->small_m_path < 0 || opt->small_m_path > 1)
+        return fail(PROJ_ERR_INVALID_ARG, "large_m_path, small_m_path, l2_prefetch and trigger_early must be 0 or 1");
     if (opt->pdl >= 0) g_opt_pdl.store(opt->pdl);
     g_opt_wait_us.store(opt->wait_limit_us);
     g_opt_skip_stage_plus1.store(opt->skip_stage_plus1);
     g_opt_large_m_path.store(opt->large_m_path);
     g_opt_l2_prefetch.store(opt->l2_prefetch);
     g_opt_trigger_early.store(opt->trigger_early);
+    g_opt_small_m_path.store(opt->small_m_path);
     return ok();
 }
 
@@ -671,6 +681,7 @@ proj_status proj_get_options(proj_options *opt) {
     opt->large_m_path = g_opt_large_m_path.load();
     opt->l2_prefetch = g_opt_l2_prefetch.load();
     opt->trigger_early = g_opt_trigger_early.load();
+    opt->small_m_path = g_opt_small_m_path.load();
     return ok();
 }
 

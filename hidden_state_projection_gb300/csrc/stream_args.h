@@ -5,7 +5,7 @@
 
 namespace hsp {
 
-enum Compute : int { kMmaBf16 = 0, kMmaTf32 = 1, kFmaFp32 = 2 };
+enum Compute : int { kMmaBf16 = 0, kMmaTf32 = 1, kFmaFp32 = 2, kFmaBf16 = 3 };
 
 constexpr int kMaxSplits = 8;
 constexpr int kDeviceErrTimeout = 7;  // same value as PROJ_ERR_TIMEOUT

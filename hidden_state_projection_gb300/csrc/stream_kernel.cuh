@@ -173,30 +173,49 @@ __device__ __forceinline__ void unit_mma(const StageView &v, uint32_t ub, int wr
     }
 }
 
-// FP32 FMA, few tokens (MT == 1): lane = (row group g = lane/8, 16-byte chunk c = lane%8).
-// Each lane owns rows wr*RT*16 + g + 4i (i < 4RT) for the 8 token slots and the
-// 4 consecutive k of chunk c; the 8 chunk lanes are added by a fixed butterfly
-// at the end.  acc[i][t]: row i, token t.
-template <class C, int RT>
+// FMA, few tokens (MT == 1), fp32 or bf16 elements: lane = (row group g = lane/8,
+// 16-byte chunk c = lane%8).  Each lane owns rows wr*RT*16 + g + 4i (i < 4RT) for
+// the first TOK token slots and the 4 (fp32) or 8 (bf16) consecutive k of chunk c;
+// the 8 chunk lanes are added by a fixed butterfly at the end.  Only tokens below M
+// are loaded and multiplied.  acc[i][t]: row i, token t.
+__device__ __forceinline__ void unpack16(const uint4 &u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack16(const uint4 &u, float (&f)[8]) {
+    // bf16 pairs: the low half is the first element (the top 16 bits of an fp32)
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    f[4] = __uint_as_float(u.z << 16);
+    f[5] = __uint_as_float(u.z & 0xFFFF0000u);
+    f[6] = __uint_as_float(u.w << 16);
+    f[7] = __uint_as_float(u.w & 0xFFFF0000u);
+}
+
+template <class C, int RT, int TOK>
 __device__ __forceinline__ void unit_fma_ksplit(const StageView &v, uint32_t ub, int wr, int lane, int M,
                                                 float (&acc)[4 * RT][8]) {
+    constexpr int E = (C::kCompute == kFmaBf16) ? 8 : 4;  // elements per 16-byte chunk
     const int c = lane & 7, g = lane >> 3;
     const uint32_t cb = ub + c * 16;
-    float4 xv[8];
+    float xf[TOK][E];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) xv[t] = lds128(v.xrow(t) + cb);
+    for (int t = 0; t < TOK; ++t)
+        if (t < M) unpack16(lds128u(v.xrow(t) + cb), xf[t]);
 #pragma unroll
     for (int i = 0; i < 4 * RT; ++i) {
-        const float4 wv = lds128(v.wrow(wr * RT * 16 + g + 4 * i) + cb);
+        float wf[E];
+        unpack16(lds128u(v.wrow(wr * RT * 16 + g + 4 * i) + cb), wf);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
+        for (int t = 0; t < TOK; ++t)
             if (t < M) {
-                acc[i][t] = fmaf(wv.x, xv[t].x, acc[i][t]);
-                acc[i][t] = fmaf(wv.y, xv[t].y, acc[i][t]);
-                acc[i][t] = fmaf(wv.z, xv[t].z, acc[i][t]);
-                acc[i][t] = fmaf(wv.w, xv[t].w, acc[i][t]);
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[i][t] = fmaf(wf[e], xf[t][e], acc[i][t]);
             }
-        }
     }
 }
 
@@ -247,7 +266,7 @@ __device__ __forceinline__ void store_out(const StreamArgs &a, int n, int tok, f
 #pragma unroll 1
     while (i + 1 < a.splits.count && n >= a.splits.off[i + 1]) ++i;
     const int64_t idx = static_cast<int64_t>(tok) * a.splits.rows[i] + (n - a.splits.off[i]);
-    if constexpr (COMPUTE == kMmaBf16) {
+    if constexpr (COMPUTE == kMmaBf16 || COMPUTE == kFmaBf16) {
         static_cast<__nv_bfloat16 *>(a.splits.out[i])[idx] = __float2bfloat16_rn(v);
     } else {
         static_cast<float *>(a.splits.out[i])[idx] = v;
@@ -291,9 +310,10 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     __syncthreads();
     if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
 
-    constexpr int kChains = (COMPUTE != kFmaFp32 && MT == 1) ? 2 : 1;
-    float acc_mma[kChains][(COMPUTE == kFmaFp32) ? 1 : RT][(COMPUTE == kFmaFp32) ? 1 : MT][4];
-    float acc_fk[(COMPUTE == kFmaFp32 && MT == 1) ? 4 * RT : 1][8];
+    constexpr bool kFma = (COMPUTE == kFmaFp32 || COMPUTE == kFmaBf16);
+    constexpr int kChains = (!kFma && MT == 1) ? 2 : 1;
+    float acc_mma[kChains][kFma ? 1 : RT][kFma ? 1 : MT][4];
+    float acc_fk[(kFma && MT == 1) ? 4 * RT : 1][8];
     float acc_fo[(COMPUTE == kFmaFp32 && MT > 1) ? 4 * RT : 1][MT];
 #pragma unroll
     for (int i = 0; i < (int)(sizeof(acc_mma) / sizeof(float)); ++i) (&acc_mma[0][0][0][0])[i] = 0.f;
@@ -393,9 +413,11 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                     zeroed = true;
                 }
                 if (!has_rows) continue;
-                if constexpr (COMPUTE == kFmaFp32) {
+                if constexpr (COMPUTE == kFmaBf16) {
+                    unit_fma_ksplit<C, RT, 2>(v, ub, wr, lane, a.M, acc_fk);
+                } else if constexpr (COMPUTE == kFmaFp32) {
                     if constexpr (MT == 1)
-                        unit_fma_ksplit<C, RT>(v, ub, wr, lane, a.M, acc_fk);
+                        unit_fma_ksplit<C, RT, 8>(v, ub, wr, lane, a.M, acc_fk);
                     else
                         unit_fma_outer<C, RT, MT>(v, ub, wr, lane, acc_fo);
                 } else {
@@ -452,7 +474,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     float *red = reinterpret_cast<float *>(smem);
     if (warp < C::kNCW && !aborted) {
         const int wk = warp % WK, wr = warp / WK;
-        if constexpr (COMPUTE == kFmaFp32) {
+        if constexpr (kFma) {
             if constexpr (MT == 1) {
                 const int c = lane & 7, g = lane >> 3;
 #pragma unroll

@@ -102,13 +102,16 @@ typedef struct {
      * tinygemm2).  Safe only for consumers that call griddepcontrol.wait; used by the
      * PDL ordering test as its positive control. */
     int32_t trigger_early;
-    int32_t reserved[2];
+    /* bf16 with M <= 2: 0 (default) = mma.sync like 3 <= M <= 8; 1 = fp32 FMA on the
+     * CUDA cores.  Both within tolerance, each bitwise self-consistent. */
+    int32_t small_m_path;
+    int32_t reserved[1];
 } proj_options;
 
 /* Kernel geometry chosen for one launch (proj_describe_plan). */
 typedef struct {
     int32_t bucket;        /* 0: M <= 8, 1: 9 <= M <= 32, 2: 33 <= M <= 64 */
-    int32_t compute;       /* 0 bf16 tensor cores, 1 tf32 tensor cores, 2 fp32 FMA */
+    int32_t compute;       /* 0 bf16 tensor cores, 1 tf32 tensor cores, 2 fp32 FMA, 3 bf16 data with fp32 FMA */
     int32_t rows_per_cta;  /* R: output rows owned by one CTA */
     int32_t row_ctas;      /* CTAs along the rows (grid.x) */
     int32_t slices;        /* S: K slices = CTAs per cluster (grid.y) */

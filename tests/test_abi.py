@@ -135,12 +135,12 @@ def test_pack_check_and_options(hsp):
     assert lib.proj_pack_check(base, base, 1280, 513, 1792, K, 0) == 0
     hsp.set_options(pdl=False, wait_limit_us=5, skip_stage=3)
     assert hsp.get_options() == {"pdl": 0, "wait_limit_us": 5, "skip_stage_plus1": 4,
-                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0}
+                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0, "small_m_path": 0}
     hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None, large_m_path=1, l2_prefetch=True)
     assert hsp.get_options()["large_m_path"] == 1 and hsp.get_options()["l2_prefetch"] == 1
     hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None)
     assert hsp.get_options() == {"pdl": 1, "wait_limit_us": 0, "skip_stage_plus1": 0,
-                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0}
+                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0, "small_m_path": 0}
     with pytest.raises(hsp.ProjError):
         hsp.set_options(wait_limit_us=-1)
 

@@ -152,3 +152,18 @@ def test_large_m_streaming_engine_matches_oracle(hsp, M):
         hsp.set_options(pdl=True, large_m_path=0)
     assert hsp.describe_plan(M, K, sum(splits), 0)["engine"] == 1
     check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"stream M{M}")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_bf16_fma_small_m_path_matches_oracle(hsp, M):
+    """The opt-in CUDA-core path for bf16 with one or two tokens."""
+    K, splits = 5120, (1280, 512)
+    x, ws = W.random_case(K, splits, M, "bf16", seed=700 + M)
+    w_cat = torch.cat(ws, 0)
+    hsp.set_options(pdl=True, small_m_path=1)
+    try:
+        assert hsp.describe_plan(M, K, sum(splits), 0)["compute"] == 3
+        outs = _run_both(hsp, x, w_cat, splits)
+    finally:
+        hsp.set_options(pdl=True, small_m_path=0)
+    check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"bf16 fma M{M}")
