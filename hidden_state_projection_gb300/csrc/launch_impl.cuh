@@ -23,6 +23,9 @@ cudaError_t launch_variant(const LaunchReq &r) {
     if (!configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
         if (e != cudaSuccess) return e;
+        // clusters of 16 K slices (fp32 rows with many tokens) exceed the portable 8
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
         configured[dev].store(1, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};

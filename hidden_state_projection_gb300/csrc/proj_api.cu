@@ -81,7 +81,7 @@ struct DeviceInfo {
     int sms = 0;
     int cc_ok = 0;
     int *err_word = nullptr;
-    int cluster_ctas[5] = {0, 0, 0, 0, 0};  // CTAs co-resident in clusters of 1, 2, 4 (index = size)
+    int cluster_ctas[17] = {0};  // CTAs co-resident in clusters of 1, 2, 4, 8, 16 (index = size)
 };
 
 // Shape of the streaming kernels for the co-residency query: one CTA of 288
@@ -91,6 +91,11 @@ __global__ void hsp_cluster_probe_kernel(int *p) {
 }
 
 int co_resident_ctas(int cluster, int fallback) {
+    if (cluster > 8 &&
+        cudaFuncSetAttribute(hsp_cluster_probe_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fallback;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, static_cast<unsigned>(cluster * 16), 1);
     cfg.blockDim = dim3(288, 1, 1);
@@ -134,6 +139,8 @@ proj_status device_info(DeviceInfo *out) {
         if (d.cc_ok) {
             d.cluster_ctas[2] = co_resident_ctas(2, d.sms);
             d.cluster_ctas[4] = co_resident_ctas(4, d.sms);
+            d.cluster_ctas[8] = co_resident_ctas(8, d.sms * 3 / 4);
+            d.cluster_ctas[16] = co_resident_ctas(16, d.sms * 2 / 3);
             void *p = nullptr;
             if ((e = cudaGetSymbolAddress(&p, g_hsp_device_error)) != cudaSuccess)
                 return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
@@ -196,7 +203,11 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     // token rows of X would not fit next to a useful weight stage otherwise.
     const int per_warp = ceil_div(p->units_total, p->WK);
     p->S = 1;
-    if (p->bucket > 0) {
+    if (p->bucket > 0 && esz == 4 && p->units_total >= 128) {
+        // fp32 rows of 16 KB and more with many tokens: every row tile re-reads its K
+        // slice of all token rows, so slices must be short -- sixteen of them
+        p->S = 16;
+    } else if (p->bucket > 0) {
         if (per_warp >= 16) p->S = 4;
         else if (per_warp >= 4) p->S = 2;
     } else if (esz == 4 && per_warp >= 16) {
@@ -204,10 +215,18 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
         // long per-warp chains; four K slices per row instead (fixed per K and dtype)
         p->S = 4;
     }
-    p->units_per_slice = ceil_div(ceil_div(p->units_total, p->S), p->WK) * p->WK;
+    // Units per slice: a multiple of WK when that leaves no slice empty (balanced
+    // warps), else the plain share.  S stays a power of two (it must divide the
+    // CTA's row slots for the cluster reduction).
+    auto slice_units = [&](int S) {
+        const int plain = ceil_div(p->units_total, S);
+        const int rounded = ceil_div(plain, p->WK) * p->WK;
+        return (S - 1) * rounded < p->units_total ? rounded : plain;
+    };
+    p->units_per_slice = slice_units(p->S);
     while (p->S > 1 && (p->S - 1) * p->units_per_slice >= p->units_total) {  // no empty slice
-        --p->S;
-        p->units_per_slice = ceil_div(ceil_div(p->units_total, p->S), p->WK) * p->WK;
+        p->S /= 2;
+        p->units_per_slice = slice_units(p->S);
     }
     const int max_rows = p->WR * 2 * 16;
     // rows per CTA: spread over the CTAs that can be resident at once (clusters of
@@ -629,15 +648,15 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
     proj_status st = check_shape(M, K, n_rows, dtype);
     if (st != PROJ_OK) return st;
     if (M < 1 || n_rows < 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "M and n_rows must be at least 1");
-    // Without a usable device the plan assumes a GB300: 152 SMs, 152 / 152 / 144
-    // CTAs co-resident in clusters of 1 / 2 / 4.
-    int ctas[5] = {0, 152, 152, 0, 144};
+    // Without a usable device the plan assumes a GB300: 152 SMs, 152 / 152 / 144 /
+    // 120 / 112 CTAs co-resident in clusters of 1 / 2 / 4 / 8 / 16.
+    int ctas[17] = {0, 152, 152, 0, 144, 0, 0, 0, 120, 0, 0, 0, 0, 0, 0, 0, 112};
     {
         char saved[sizeof g_last_error];
         memcpy(saved, g_last_error, sizeof saved);
         DeviceInfo d;
         if (device_info(&d) == PROJ_OK)
-            for (int k = 1; k < 5; ++k) ctas[k] = d.cluster_ctas[k];
+            for (int k = 1; k < 17; ++k) ctas[k] = d.cluster_ctas[k];
         else
             (void)cudaGetLastError();
         memcpy(g_last_error, saved, sizeof saved);
