@@ -374,14 +374,16 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, UPlan *p) {
     p->tiles = ceil_div(n_rows, 128);
     p->x_box = p->NT * 128;
     p->stage_bytes = 16384 + p->x_box;
-    int ring = (110 * 1024) / p->stage_bytes;
+    // receive buffer of the cluster reduction (dedicated); the staging buffer aliases
+    // the ring.  Two CTAs per SM: ring + receive buffer within ~110 KB.
+    const int red_bytes = 128 * (p->NT + 4) * 4;
+    const int recv_bytes = p->S > 1 ? red_bytes : 0;
+    int ring = (110 * 1024 - recv_bytes) / p->stage_bytes;
     if (ring < 2) ring = 2;
     if (ring > p->kb_per_slice) ring = p->kb_per_slice < 2 ? 2 : p->kb_per_slice;
-    // the ring also holds the cluster reduction's staging and receive buffers
-    const int reduce_bytes = 2 * 128 * (p->NT + 4) * 4;
-    while (p->S > 1 && ring * p->stage_bytes < reduce_bytes) ++ring;
+    while (p->S > 1 && ring * p->stage_bytes < red_bytes) ++ring;
     p->ring = ring;
-    p->smem = 1024 + ring * p->stage_bytes + (2 * ring + 1) * 8 + 16 + 64;
+    p->smem = 1024 + ring * p->stage_bytes + recv_bytes + (2 * ring + 2) * 8 + 16 + 64;
     proj_plan_info &i = p->info;
     i.bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
     i.compute = p->compute;

@@ -17,9 +17,10 @@
 //     K = 16 bf16 or 8 tf32 each) per k-block into one TMEM accumulator and commits
 //     each stage back to the ring; a final commit marks the accumulator ready;
 //   * all four warps read the accumulator (warp w owns TMEM lanes 32w..32w+31, one
-//     weight row per thread), then either store (S = 1) or push the partials of
-//     each owner's rows into that CTA's shared memory (coalesced st.shared::cluster),
-//     and the owner adds the S slices in slice order and stores.  The sum of every
+//     weight row per thread), then either store (S = 1) or stage the partials per
+//     owner CTA and bulk-copy each owner's block into its receive buffer (a copy
+//     between cluster shared memories, counted on the owner's mbarrier); the owner
+//     adds the S slices in slice order and stores.  The sum of every
 //     output is the tensor-core accumulation over K in order, then slices in order:
 //     a function of (K, dtype, M bucket) only, never of the row's place in a tile.
 //   * the trigger follows a release fence in every storing thread (TensorRT-LLM PR
@@ -80,14 +81,19 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t ring = smem_u32(smem);
+    constexpr int kPitch = NT + 4;                       // row pitch (floats) of the reduction buffers
+    constexpr uint32_t kRedBytes = 128u * kPitch * 4u;  // one partial per weight row of the tile
     const uint32_t ring_bytes = a.ring_stages * a.stage_bytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ring_bytes);
+    float *recv = reinterpret_cast<float *>(smem + ring_bytes);  // K-slice partials of my rows (S > 1)
+    const uint32_t recv_bytes = a.slices > 1 ? kRedBytes : 0u;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + ring_bytes + recv_bytes);
     uint64_t *empty = full + a.ring_stages;
     uint64_t *accf = empty + a.ring_stages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
+    uint64_t *recv_bar = accf + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(recv_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *issued = const_cast<int *>(abort_flag) + 1;  // k-blocks whose copies were issued
-    float *red = reinterpret_cast<float *>(smem);      // receive buffer of the cluster reduction
+    float *staging = reinterpret_cast<float *>(smem);  // my partials, one block per owner (aliases the ring)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row0 = blockIdx.x * 128;
@@ -102,6 +108,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
         }
         mbar_init(smem_u32(accf), 1);
+        mbar_init(smem_u32(recv_bar), 1);
+        // every slice's block of my rows arrives on recv_bar: expect all of them now
+        if (a.slices > 1) mbar_arrive_expect_tx(smem_u32(recv_bar), kRedBytes);
         *abort_flag = 0;
         *issued = 0;
         mbar_fence_init();
@@ -115,6 +124,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_d = *tmem_slot;
     if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
+    // First half of a cluster barrier: the peers' receive barriers are initialised
+    // before anyone pushes into them (the wait comes after the main loop).
+    if (a.slices > 1) cluster_arrive();
 
     if (warp >= 2 && a.prefetch_l2 && nkb > 0) {
         // One contiguous run per weight row: this slice's k-blocks of that row.
@@ -248,51 +260,48 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             stored = true;
         }
     } else {
-        // Push model.  Each thread first puts its row's partial into a local staging
-        // buffer laid out as one contiguous block per owner CTA, [owner][row][token]
-        // with a row pitch of NT + 4 floats; after the first cluster barrier (every CTA
-        // has left its ring, which both buffers alias) the CTA copies block q into the
-        // receive buffer of CTA q with coalesced remote stores (consecutive lanes,
-        // consecutive 16 bytes; remote stores do not wait).  After the second barrier
-        // each owner adds the S slices of its rows in slice order from local memory.
-        constexpr int kPitch = NT + 4;
+        // Push model.  Each thread puts its row's partial into a local staging buffer
+        // laid out as one contiguous block per owner CTA, [owner][row][token] with a
+        // row pitch of NT + 4 floats.  One thread then bulk-copies block q into the
+        // dedicated receive buffer of CTA q, completing on that CTA's receive barrier,
+        // which has expected all S blocks since the kernel started.  Each owner waits
+        // for its barrier and adds the S slices of its rows in slice order.
         const int per = 128 / a.slices;
-        const int block = per * kPitch;                 // floats per owner block
-        float *staging = red;
-        float *recv = red + 128 * kPitch;
+        const uint32_t block_bytes = static_cast<uint32_t>(per * kPitch * 4);
         {
             const int q = r / per, rr = r - q * per;
-            float *dst = staging + q * block + rr * kPitch;
+            float *dst = staging + q * per * kPitch + rr * kPitch;
 #pragma unroll
             for (int c = 0; c < NT; c += 4) *reinterpret_cast<float4 *>(dst + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
         }
+        fence_proxy_async_smem();   // staging writes -> the bulk copies that read them
         __syncthreads();
-        cluster_sync_all();
-        {
-            const uint32_t recv_local = smem_u32(recv);
-            const int chunks = block / 4;               // 16-byte chunks per owner block
-            for (int c = tid; c < a.slices * chunks; c += kUmmaThreads) {
-                const int q = c / chunks, off = c - q * chunks;
-                const float4 val = *reinterpret_cast<const float4 *>(staging + q * block + off * 4);
-                const uint32_t dst = recv_local + static_cast<uint32_t>((slice * block + off * 4) * 4);
-                st_shared_cluster_v4(cluster_map_shared(dst, static_cast<uint32_t>(q)), val.x, val.y, val.z, val.w);
-            }
+        cluster_wait();             // every peer's receive barrier is initialised
+        if (tid == 0) {
+            const uint32_t recv_local = smem_u32(recv), bar_local = smem_u32(recv_bar), src = smem_u32(staging);
+            for (int q = 0; q < a.slices; ++q)
+                bulk_s2s_cluster(cluster_map_shared(recv_local + slice * block_bytes, static_cast<uint32_t>(q)),
+                                 src + q * block_bytes, block_bytes, cluster_map_shared(bar_local, static_cast<uint32_t>(q)));
         }
-        cluster_sync_all();
-        if (!aborted) {
+        const bool got = umma_wait(smem_u32(recv_bar), 0u, a.wait_limit_ns, abort_flag);
+        if (!got && tid == 0) {
+            atomicCAS(a.err_word, 0, kDeviceErrTimeout);
+            *abort_flag = 1;
+        }
+        if (!aborted && got) {
             constexpr int kT4 = NT / 4;
             // consecutive threads take consecutive rows of the same four tokens
             for (int e = tid; e < per * kT4; e += kUmmaThreads) {
                 const int t4 = (e / per) * 4, rr = e - (e / per) * per;
                 const int row = slice * per + rr;
                 if (row >= rows_here || t4 >= a.M) continue;
-                float4 part[8];
+                float4 part[16];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (q < a.slices) part[q] = *reinterpret_cast<const float4 *>(recv + q * block + rr * kPitch + t4);
+                for (int q = 0; q < 16; ++q)
+                    if (q < a.slices) part[q] = *reinterpret_cast<const float4 *>(recv + (q * per + rr) * kPitch + t4);
                 float4 acc = part[0];
 #pragma unroll
-                for (int q = 1; q < 8; ++q)
+                for (int q = 1; q < 16; ++q)
                     if (q < a.slices) {
                         acc.x += part[q].x;
                         acc.y += part[q].y;
@@ -310,11 +319,15 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     if (stored) fence_release_gpu();
     tc_fence_before_sync();
     __syncthreads();
+    // Every output store of this CTA is performed: trigger the dependent launch.
+    griddep_launch_dependents();
     if (warp == 2) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_d, C::kTmemCols);
     }
-    griddep_launch_dependents();
+    // No CTA leaves while a peer's bulk copy may still read its staging buffer: every
+    // CTA arrives here only after its own receive barrier completed.
+    if (a.slices > 1) cluster_sync_all();
 }
 
 }  // namespace hsp
