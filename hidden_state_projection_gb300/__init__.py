@@ -57,7 +57,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "bucket", "compute", "rows_per_cta", "row_ctas", "slices", "k_warps", "row_warps",
         "row_tiles", "token_tiles", "ring_stages", "stage_bytes", "smem_bytes", "k_per_stage",
-        "stages_total", "threads", "units_per_slice", "engine")] + [("reserved", ctypes.c_int32 * 3)]
+        "stages_total", "threads", "units_per_slice", "engine", "tensor_copies")] + [("reserved", ctypes.c_int32 * 2)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_ if n != "reserved"}

@@ -13,10 +13,13 @@ struct LaunchReq {
     int bucket;      // 0: (WR, WK) = (1, 8); 1: (2, 4); 2: (4, 2)
     int MT;          // token tiles of 8
     int RT;          // 16-row tiles per warp
+    int tensor;      // 1: 3-D tensor copies (tmap_w / tmap_x used), 0: 1-D bulk copies
     dim3 grid;       // (row CTAs, slices, 1)
     int smem_bytes;  // dynamic shared memory
     int pdl;         // programmatic stream serialization
     cudaStream_t stream;
+    CUtensorMap tmap_w;  // weights viewed as [units][rows][128 bytes], box [stage units][R][128 bytes]
+    CUtensorMap tmap_x;  // tokens viewed as [units][M][128 bytes], box [stage units][M][128 bytes]
     StreamArgs args;
 };
 

@@ -11,9 +11,9 @@ namespace hsp {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxDynamicSmem = 232448;  // 227 KiB, the per-block opt-in limit of sm_103
 
-template <int COMPUTE, int MT, int RT, int WR, int WK>
-cudaError_t launch_variant(const LaunchReq &r) {
-    auto kern = hsp_stream_kernel<COMPUTE, MT, RT, WR, WK>;
+template <int COMPUTE, int MT, int RT, int WR, int WK, bool TENSOR>
+cudaError_t launch_one(const LaunchReq &r) {
+    auto kern = hsp_stream_kernel<COMPUTE, MT, RT, WR, WK, TENSOR>;
     // The shared-memory opt-in is per function and per device; set it once.
     static std::atomic<unsigned char> configured[kMaxDevices];
     int dev = 0;
@@ -49,7 +49,12 @@ cudaError_t launch_variant(const LaunchReq &r) {
     }
     cfg.attrs = attrs;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, kern, r.args);
+    return cudaLaunchKernelEx(&cfg, kern, r.tmap_w, r.tmap_x, r.args);
+}
+
+template <int COMPUTE, int MT, int RT, int WR, int WK>
+cudaError_t launch_variant(const LaunchReq &r) {
+    return r.tensor ? launch_one<COMPUTE, MT, RT, WR, WK, true>(r) : launch_one<COMPUTE, MT, RT, WR, WK, false>(r);
 }
 
 template <int COMPUTE>

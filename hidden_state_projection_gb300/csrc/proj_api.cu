@@ -16,9 +16,11 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -32,7 +34,8 @@ using hsp::LaunchReq;
 using hsp::StreamArgs;
 
 constexpr int kSmemLimit = 232448;          // per-block dynamic shared memory on sm_103
-constexpr int kSmemReserve = 128 + 512;     // ring alignment slack + barriers + flags
+constexpr int kSmemReserve = 1024 + 512;    // ring alignment slack (1024 for the swizzle) + barriers + flags
+constexpr int kStageWeightBytes = 65536;    // tensor layout: weight bytes per ring stage
 constexpr int kMaxRingStages = 32;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
@@ -161,7 +164,8 @@ struct Plan {
     proj_plan_info info;
     int compute, bucket, MT, RT, WR, WK, S, R, grid_x;
     int units_total, units_per_slice, stage_units, stages_per_slice, ring_stages;
-    int pitch, stage_bytes, ring_bytes, smem;
+    int tensor;  // 3-D tensor copies (rows a multiple of 128 bytes) or 1-D bulk copies
+    int pitch, stage_bytes, x_off, ring_bytes, smem;
 };
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -182,9 +186,11 @@ proj_status check_shape(int32_t M, int32_t K, int64_t n_total, int dt) {
 //   - bucket, WK, S and units_per_slice depend on (M's bucket, K, dtype) only:
 //     they fix which warp and which K slice sums every 128-byte unit of K, hence
 //     the summation order of every output;
-//   - R (rows per CTA) spreads the rows over the SMs and the stage width is the
-//     widest that still leaves two ring stages in shared memory: long contiguous
-//     row segments per bulk copy.  Neither changes the order.
+//   - R (rows per CTA) spreads the rows over the SMs.  With tensor copies (rows a
+//     multiple of 128 bytes) a stage holds ~16 KB of weights, so the compute left
+//     after the last byte lands is short; with bulk copies the stage width is the
+//     widest that still leaves two ring stages in shared memory (long contiguous
+//     row segments per copy).  Neither changes the order.
 void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas, Plan *p) {
     memset(p, 0, sizeof *p);
     const int esz = elem_size(dt);
@@ -242,29 +248,62 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     const int red_bytes = p->WK * slots * 8 * p->MT * 4 + (p->S > 1 ? slots * 8 * p->MT * 4 : 0);
     const int budget = kSmemLimit - kSmemReserve;
     const int Us = p->units_per_slice;
-    const int first = Us >= 2 * p->WK ? 2 : 1;
-    for (int nst = first; nst <= Us; ++nst) {
-        int su = ceil_div(Us, nst);
-        if (su > p->WK) su = ceil_div(su, p->WK) * p->WK;
-        const int n_eff = ceil_div(Us, su);
-        const int pitch = su * hsp::kUnitBytes + 16;
-        const int stage = (p->R + M) * pitch;
-        int ring = budget / stage;
-        if (ring > n_eff) ring = n_eff;
-        if (ring > kMaxRingStages) ring = kMaxRingStages;
-        if (ring >= (n_eff >= 2 ? 2 : 1) && ring * stage >= 0) {
-            p->stage_units = su;
-            p->stages_per_slice = n_eff;
-            p->ring_stages = ring;
-            p->pitch = pitch;
-            p->stage_bytes = stage;
-            break;
+    p->tensor = (row_bytes % hsp::kUnitBytes) == 0;
+    if (p->tensor) {
+        // Stages of su units, su dividing the slice (no box reaches into the next
+        // slice), a multiple of WK where possible (every warp gets the same share),
+        // holding about kStageWeightBytes of weights.  One weight box and one token
+        // box per stage, each rounded up to 1024 bytes.
+        auto box = [](int rows, int su) { return ceil_div(rows * su * hsp::kUnitBytes, 1024) * 1024; };
+        const int target = std::max(1, kStageWeightBytes / (p->R * hsp::kUnitBytes));
+        // the divisor of the slice nearest the target (the larger one on a tie), at
+        // most half the slice: at least two stages, so loads and products overlap
+        int su = 0;
+        for (int d = 1; d <= std::max(1, Us / 2); ++d)
+            if (Us % d == 0 && (su == 0 || std::abs(d - target) <= std::abs(su - target))) su = d;
+        for (;;) {
+            const int stage = box(p->R, su) + box(M, su);
+            const int nst = ceil_div(Us, su);
+            int ring = std::min(std::min(nst, budget / stage), kMaxRingStages);
+            if (ring >= std::min(2, nst) || su == 1) {
+                p->stage_units = su;
+                p->stages_per_slice = nst;
+                p->ring_stages = ring;
+                p->pitch = 0;
+                p->stage_bytes = stage;
+                p->x_off = box(p->R, su);
+                break;
+            }
+            int d = su - 1;  // next smaller divisor of the slice
+            while (d > 1 && Us % d != 0) --d;
+            su = d;
+        }
+    } else {
+        const int first = Us >= 2 * p->WK ? 2 : 1;
+        for (int nst = first; nst <= Us; ++nst) {
+            int su = ceil_div(Us, nst);
+            if (su > p->WK) su = ceil_div(su, p->WK) * p->WK;
+            const int n_eff = ceil_div(Us, su);
+            const int pitch = su * hsp::kUnitBytes + 16;
+            const int stage = (p->R + M) * pitch;
+            int ring = budget / stage;
+            if (ring > n_eff) ring = n_eff;
+            if (ring > kMaxRingStages) ring = kMaxRingStages;
+            if (ring >= (n_eff >= 2 ? 2 : 1)) {
+                p->stage_units = su;
+                p->stages_per_slice = n_eff;
+                p->ring_stages = ring;
+                p->pitch = pitch;
+                p->stage_bytes = stage;
+                p->x_off = p->R * pitch;
+                break;
+            }
         }
     }
     p->ring_bytes = p->ring_stages * p->stage_bytes;
     if (p->ring_bytes < red_bytes) p->ring_bytes = red_bytes;
     p->ring_bytes = ceil_div(p->ring_bytes, 128) * 128;
-    p->smem = 128 + p->ring_bytes + 2 * p->ring_stages * 8 + 8 + 4 * p->ring_stages + 64;
+    p->smem = 1024 + p->ring_bytes + 2 * p->ring_stages * 8 + 8 + 4 * p->ring_stages + 64;
     proj_plan_info &i = p->info;
     i.bucket = p->bucket;
     i.compute = p->compute;
@@ -282,6 +321,7 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     i.stages_total = p->stages_per_slice;
     i.threads = hsp::kThreadsPerCta;
     i.units_per_slice = p->units_per_slice;
+    i.tensor_copies = p->tensor;
 }
 
 // ---- tensor maps (tensor-memory kernel only) ---------------------------------
@@ -290,8 +330,10 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
 struct MapEntry {
-    uint64_t ptr, d0, d1, box0, box1;
-    int dtype;
+    uint64_t ptr;
+    int rank, dtype;
+    uint64_t dims[3], strides[2];
+    uint32_t box[3];
     bool used;
     CUtensorMap map;
 };
@@ -300,10 +342,11 @@ std::mutex g_map_mu;
 MapEntry g_maps[kMapCache];
 int g_map_next = 0;
 
-// 2-D map over a row-major [d1, d0] matrix (d0 contiguous), box [box1 rows, box0
-// elements] = 128 bytes wide, 128-byte swizzle, zero fill outside the matrix.
-proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0, uint32_t box1, proj_dtype dt,
-                       CUtensorMap *out) {
+// Tiled tensor map (128-byte swizzle, zero fill past the tensor), cached per
+// (pointer, shape, box).  dims[0] is the innermost extent in elements; strides[i]
+// is the byte stride of dimension i + 1.
+proj_status encode_map(const void *ptr, int rank, const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                       proj_dtype dt, CUtensorMap *out) {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -315,37 +358,65 @@ proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0,
             (void)cudaGetLastError();
     });
     if (!g_encode) return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const uint64_t key = reinterpret_cast<uint64_t>(ptr);
+    MapEntry key{};
+    key.ptr = reinterpret_cast<uint64_t>(ptr);
+    key.rank = rank;
+    key.dtype = static_cast<int>(dt);
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides[i];
+    }
+    auto same = [&](const MapEntry &m) {
+        if (!m.used || m.ptr != key.ptr || m.rank != key.rank || m.dtype != key.dtype) return false;
+        for (int i = 0; i < rank; ++i) {
+            if (m.dims[i] != key.dims[i] || m.box[i] != key.box[i]) return false;
+            if (i + 1 < rank && m.strides[i] != key.strides[i]) return false;
+        }
+        return true;
+    };
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
-        for (int i = 0; i < kMapCache; ++i) {
-            const MapEntry &m = g_maps[i];
-            if (m.used && m.ptr == key && m.d0 == d0 && m.d1 == d1 && m.box0 == box0 && m.box1 == box1 &&
-                m.dtype == static_cast<int>(dt)) {
-                *out = m.map;
+        for (int i = 0; i < kMapCache; ++i)
+            if (same(g_maps[i])) {
+                *out = g_maps[i].map;
                 return PROJ_OK;
             }
-        }
     }
     CUtensorMap map;
-    cuuint64_t dims[2] = {d0, d1};
-    cuuint64_t strides[1] = {d0 * static_cast<uint64_t>(elem_size(dt))};
-    cuuint32_t box[2] = {box0, box1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(&map, dt == PROJ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                          const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], estr[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = g_encode(&map, dt == PROJ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), d, st, b, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
-        return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu], box [%u x %u]",
-                    static_cast<int>(r), (unsigned long long)d1, (unsigned long long)d0, box1, box0);
+        return fail(PROJ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d): rank %d, dims [%llu %llu %llu], box [%u %u %u]",
+                    static_cast<int>(r), rank, (unsigned long long)d[0], (unsigned long long)(rank > 1 ? d[1] : 0),
+                    (unsigned long long)(rank > 2 ? d[2] : 0), b[0], rank > 1 ? b[1] : 0u, rank > 2 ? b[2] : 0u);
     {
         std::lock_guard<std::mutex> lk(g_map_mu);
-        g_maps[g_map_next] = MapEntry{key, d0, d1, box0, box1, static_cast<int>(dt), true, map};
+        key.used = true;
+        key.map = map;
+        g_maps[g_map_next] = key;
         g_map_next = (g_map_next + 1) % kMapCache;
     }
     *out = map;
     return PROJ_OK;
+}
+
+// 2-D map of a row-major [d1, d0] tensor, box [box1, box0].
+proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0, uint32_t box1, proj_dtype dt,
+                       CUtensorMap *out) {
+    const uint64_t dims[2] = {d0, d1};
+    const uint64_t strides[1] = {d0 * static_cast<uint64_t>(elem_size(dt))};
+    const uint32_t box[2] = {box0, box1};
+    return encode_map(ptr, 2, dims, strides, box, dt, out);
 }
 
 // ---- tensor-memory plan ----------------------------------------------------
@@ -457,6 +528,22 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
     if (p.ring_stages < 1 || p.smem > kSmemLimit)
         return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "no shared-memory plan for M=%d K=%d rows=%d", M, K, n_rows);
     LaunchReq r{};
+    if (p.tensor) {
+        // weights as [units][rows][128 bytes] (row stride row_bytes, unit stride 128
+        // bytes), one box [stage units][R][128 bytes] per stage; tokens likewise
+        const uint64_t ke = 128u / static_cast<uint64_t>(elem_size(dt));
+        const uint64_t row_bytes = static_cast<uint64_t>(K) * elem_size(dt);
+        const uint64_t wdims[3] = {ke, static_cast<uint64_t>(n_rows), static_cast<uint64_t>(p.units_total)};
+        const uint64_t xdims[3] = {ke, static_cast<uint64_t>(M), static_cast<uint64_t>(p.units_total)};
+        const uint64_t strides[2] = {row_bytes, 128u};
+        const uint32_t wbox[3] = {static_cast<uint32_t>(ke), static_cast<uint32_t>(p.R), static_cast<uint32_t>(p.stage_units)};
+        const uint32_t xbox[3] = {static_cast<uint32_t>(ke), static_cast<uint32_t>(M), static_cast<uint32_t>(p.stage_units)};
+        proj_status st = encode_map(w, 3, wdims, strides, wbox, dt, &r.tmap_w);
+        if (st != PROJ_OK) return st;
+        st = encode_map(x, 3, xdims, strides, xbox, dt, &r.tmap_x);
+        if (st != PROJ_OK) return st;
+    }
+    r.tensor = p.tensor;
     r.compute = p.compute;
     r.bucket = p.bucket;
     r.MT = p.MT;
@@ -481,6 +568,7 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
     a.pitch = static_cast<uint32_t>(p.pitch);
     a.stage_bytes = static_cast<uint32_t>(p.stage_bytes);
     a.ring_bytes = static_cast<uint32_t>(p.ring_bytes);
+    a.x_off = static_cast<uint32_t>(p.x_off);
     a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
     a.trigger_early = g_opt_trigger_early.load();
     const int wus = g_opt_wait_us.load();

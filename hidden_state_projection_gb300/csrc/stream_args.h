@@ -35,7 +35,15 @@ struct SplitTable {
 // CTA that owns its K slice (slice s holds units [s*units_per_slice, ...)); a
 // ring stage carries stage_units consecutive units of every row of the CTA and
 // of every token.  Only the unit -> warp -> slice map decides the summation
-// order; the stage width and the row count do not.
+// order; the stage width, the row count and the stage layout do not.
+//
+// Two stage layouts, one per copy engine use:
+//   tensor (rows a multiple of 128 bytes): one 3-D tensor copy per stage for the
+//     weights and one for the tokens, each a box [stage_units][rows][128 bytes]
+//     with the 128-byte swizzle (16-byte chunk c of line L stored at c ^ (L mod 8));
+//     the token box starts x_off bytes (a multiple of 1024) after the weight box;
+//   bulk (any other K): one 1-D bulk copy per row and stage, rows at `pitch`
+//     (16 mod 128) bytes; the token rows start x_off = R * pitch after the weights.
 struct StreamArgs {
     const char *w;             // first weight row of the launch, [n_rows, K] row-major
     const char *x;             // activations, [M, K] row-major
@@ -49,9 +57,10 @@ struct StreamArgs {
     int32_t stages_per_slice;  // ceil(units_per_slice / stage_units)
     int32_t ring_stages;       // shared-memory ring depth
     int32_t slices;            // S (cluster size along grid.y)
-    uint32_t pitch;            // shared-memory row pitch of a stage (stage_units*128 + 16)
-    uint32_t stage_bytes;      // (R + M) * pitch
+    uint32_t pitch;            // bulk layout: shared-memory row pitch (stage_units*128 + 16)
+    uint32_t stage_bytes;      // bytes of one stage (weights + tokens)
     uint32_t ring_bytes;       // ring_stages * stage_bytes, at least the reduction buffer
+    uint32_t x_off;            // bytes from a stage's start to its first token row
     int32_t skip_stage;        // test hook: this stage of every slice is never loaded (-1: off)
     int32_t trigger_early;     // test hook: trigger dependents at kernel start
     uint64_t wait_limit_ns;    // bound of every barrier wait

@@ -11,16 +11,20 @@
 // warp order and rounded once; TensorRT-LLM PR #20502, glmFusedAGemm commit
 // message -- re-drawn for bulk-copy rings and clusters on sm_103a):
 //
-//   * a ring of shared-memory stages is filled with 1-D bulk copies: one copy per
-//     weight row and per token row, each a contiguous segment of stage_units * 128
-//     bytes (long contiguous reads keep DRAM pages open; 128-byte pieces at the
-//     row pitch do not).  All nine warps issue copies -- warp w the rows and
-//     tokens congruent to w mod 9, one lane per copy -- because one issuing
-//     thread manages only about one copy per 55-150 ns.  The weight copies of the first ring's worth of stages
-//     are issued before griddepcontrol.wait, the activation copies only after
-//     it; a slot is refilled by the same warps once every consumer has released it;
-//   * shared rows are padded to a pitch of 16 mod 128 bytes, so the eight rows
-//     an ldmatrix phase reads fall in eight different bank groups;
+//   * a ring of shared-memory stages is filled by the copy engine.  When a row is a
+//     whole number of 128-byte units (every workload of the pages), one thread of
+//     the ninth warp issues TWO 3-D tensor copies per stage: the weight box
+//     [stage_units][R rows][128 bytes] and the token box [stage_units][M][128 bytes],
+//     both with the 128-byte swizzle, so that the eight rows an ldmatrix phase
+//     reads sit in eight different bank groups.  The copy engine accepts about one
+//     copy per 55 cycles per SM, so one large box per stage replaces the R + M
+//     row copies of the other layout and leaves the stages short (small compute
+//     tail after the last byte).  Otherwise (a ragged last unit) each weight row
+//     and token row of a stage is one 1-D bulk copy of a contiguous segment, rows
+//     padded to a pitch of 16 mod 128 bytes, issued lane-parallel by all nine
+//     warps.  Weight copies of the first ring's worth of stages are issued before
+//     griddepcontrol.wait, token copies only after it; a slot is refilled once
+//     every consumer has released it;
 //   * consumer warp (wr, wk) takes every k-unit u (128 bytes of K) of a stage
 //     with u mod WK == wk, for its RT 16-row tiles, and accumulates in registers
 //     (mma.sync bf16 / tf32, or fp32 FMA);
@@ -37,9 +41,10 @@
 // tile, the grid or the arrival order -- so fused and per-projection launches,
 // repeated runs and graph replays give identical bits.
 //
-// Rows past the CTA's last weight row, and token rows past M, are never loaded:
-// their fragment reads are clamped to the last loaded row, and their results are
-// never stored.  A final partial k-unit is zero-filled in shared memory before use.
+// Fragment reads of rows past the CTA's last weight row, and of token rows past M,
+// are clamped to the last real row; their results are never stored.  The tensor
+// copies zero-fill rows and units past the tensor; a final partial k-unit (bulk
+// layout only) is zero-filled in shared memory before use.
 //
 // Every wait on a shared-memory barrier is bounded (globaltimer); on expiry the
 // kernel records PROJ_ERR_TIMEOUT in the device error word, stops computing,
@@ -98,17 +103,44 @@ __device__ __forceinline__ void record_timeout(int *err_word, volatile int *abor
     *abort_flag = 1;
 }
 
-// Shared-memory view of one stage: weight rows [0, R) then token rows [0, M),
-// each `pitch` bytes apart; reads past the loaded rows are clamped.
-struct StageView {
+// Shared-memory view of one stage, addressed by (row, unit of the stage, 16-byte
+// chunk of the unit).  Reads past the real rows are clamped to the last one.
+template <bool TENSOR>
+struct StageView;
+
+// Bulk layout: weight rows [0, R) then token rows, each `pitch` bytes apart.
+template <>
+struct StageView<false> {
     uint32_t w, x;     // shared addresses of weight row 0 / token row 0
     uint32_t pitch;
-    int rmax, tmax;    // last loaded weight row / token row
-    __device__ __forceinline__ uint32_t wrow(int r) const { return w + static_cast<uint32_t>(min(r, rmax)) * pitch; }
-    __device__ __forceinline__ uint32_t xrow(int t) const { return x + static_cast<uint32_t>(min(t, tmax)) * pitch; }
+    int rmax, tmax;    // last real weight row / token row
+    __device__ __forceinline__ uint32_t wa(int r, int ul, int c) const {
+        return w + static_cast<uint32_t>(min(r, rmax)) * pitch + static_cast<uint32_t>(ul * kUnitBytes + c * 16);
+    }
+    __device__ __forceinline__ uint32_t xa(int t, int ul, int c) const {
+        return x + static_cast<uint32_t>(min(t, tmax)) * pitch + static_cast<uint32_t>(ul * kUnitBytes + c * 16);
+    }
 };
 
-// ---- inner products on one 128-byte k-unit at byte offset `ub` of the stage ----
+// Tensor layout: line L = unit * rows + row of 128 bytes; chunk c of line L is stored
+// at chunk c ^ (L mod 8) (the copy engine's 128-byte swizzle; both boxes start on a
+// 1024-byte boundary).
+template <>
+struct StageView<true> {
+    uint32_t w, x;
+    int wrows, xrows;  // box rows: R and M
+    int rmax, tmax;
+    __device__ __forceinline__ uint32_t wa(int r, int ul, int c) const {
+        const int L = ul * wrows + min(r, rmax);
+        return w + static_cast<uint32_t>(L * kUnitBytes + ((c ^ (L & 7)) << 4));
+    }
+    __device__ __forceinline__ uint32_t xa(int t, int ul, int c) const {
+        const int L = ul * xrows + min(t, tmax);
+        return x + static_cast<uint32_t>(L * kUnitBytes + ((c ^ (L & 7)) << 4));
+    }
+};
+
+// ---- inner products on one 128-byte k-unit (unit `ul` of the stage) ----
 
 // Tensor cores: 4 k-steps (k16 for bf16, k8 for tf32) over the warp's row tiles.
 // All fragment loads of a batch of k-steps are issued before its products, so
@@ -117,9 +149,8 @@ struct StageView {
 // and odd k-steps feed two accumulator chains (acc[0], acc[1]) that are added at
 // the end: half the dependent MMA latency.  With more token tiles the tiles
 // themselves are independent chains.
-template <class C, int RT, int MT, int NCH>
-__device__ __forceinline__ void unit_mma(const StageView &v, uint32_t ub, int wr, int lane,
-                                         float (&acc)[NCH][RT][MT][4]) {
+template <class C, int RT, int MT, int NCH, class V>
+__device__ __forceinline__ void unit_mma(const V &v, int ul, int wr, int lane, float (&acc)[NCH][RT][MT][4]) {
     constexpr int kBatch = (MT >= 4) ? 2 : 4;
     constexpr int kMask = NCH - 1;
 #pragma unroll
@@ -128,23 +159,23 @@ __device__ __forceinline__ void unit_mma(const StageView &v, uint32_t ub, int wr
         uint32_t a[kBatch][RT][4];
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
-            const uint32_t bb = ub + (k0 + q) * 32 + ((lane >> 3) & 1) * 16;
+            const int cb = 2 * (k0 + q) + ((lane >> 3) & 1);   // 16-byte chunk of the token rows
             if constexpr (MT == 1) {
-                ldsm_x2(v.xrow(lane & 7) + bb, b[q][0][0], b[q][0][1]);
+                ldsm_x2(v.xa(lane & 7, ul, cb), b[q][0][0], b[q][0][1]);
             } else {
 #pragma unroll
                 for (int j = 0; j < MT; j += 2) {
                     const int tok = (j + (lane >> 4)) * 8 + (lane & 7);
-                    ldsm_x4(v.xrow(tok) + bb, b[q][j][0], b[q][j][1], b[q][j + 1][0], b[q][j + 1][1]);
+                    ldsm_x4(v.xa(tok, ul, cb), b[q][j][0], b[q][j][1], b[q][j + 1][0], b[q][j + 1][1]);
                 }
             }
         }
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
-            const uint32_t ab = ub + (k0 + q) * 32 + (lane >> 4) * 16;
+            const int ca = 2 * (k0 + q) + (lane >> 4);          // 16-byte chunk of the weight rows
 #pragma unroll
             for (int t = 0; t < RT; ++t)
-                ldsm_x4(v.wrow(wr * RT * 16 + t * 16 + (lane & 15)) + ab, a[q][t][0], a[q][t][1], a[q][t][2],
+                ldsm_x4(v.wa(wr * RT * 16 + t * 16 + (lane & 15), ul, ca), a[q][t][0], a[q][t][1], a[q][t][2],
                         a[q][t][3]);
         }
 #pragma unroll
@@ -196,20 +227,18 @@ __device__ __forceinline__ void unpack16(const uint4 &u, float (&f)[8]) {
     f[7] = __uint_as_float(u.w & 0xFFFF0000u);
 }
 
-template <class C, int RT, int TOK>
-__device__ __forceinline__ void unit_fma_ksplit(const StageView &v, uint32_t ub, int wr, int lane, int M,
-                                                float (&acc)[4 * RT][8]) {
+template <class C, int RT, int TOK, class V>
+__device__ __forceinline__ void unit_fma_ksplit(const V &v, int ul, int wr, int lane, int M, float (&acc)[4 * RT][8]) {
     constexpr int E = (C::kCompute == kFmaBf16) ? 8 : 4;  // elements per 16-byte chunk
     const int c = lane & 7, g = lane >> 3;
-    const uint32_t cb = ub + c * 16;
     float xf[TOK][E];
 #pragma unroll
     for (int t = 0; t < TOK; ++t)
-        if (t < M) unpack16(lds128u(v.xrow(t) + cb), xf[t]);
+        if (t < M) unpack16(lds128u(v.xa(t, ul, c)), xf[t]);
 #pragma unroll
     for (int i = 0; i < 4 * RT; ++i) {
         float wf[E];
-        unpack16(lds128u(v.wrow(wr * RT * 16 + g + 4 * i) + cb), wf);
+        unpack16(lds128u(v.wa(wr * RT * 16 + g + 4 * i, ul, c)), wf);
 #pragma unroll
         for (int t = 0; t < TOK; ++t)
             if (t < M) {
@@ -222,17 +251,16 @@ __device__ __forceinline__ void unit_fma_ksplit(const StageView &v, uint32_t ub,
 // FP32 FMA, many tokens (MT >= 2): lane = (row lane rl = lane%4, token lane
 // tl = lane/4); rows wr*RT*16 + rl + 4i (i < 4RT), tokens tl + 8j (j < MT); each
 // output is one sequential fma chain over k.
-template <class C, int RT, int MT>
-__device__ __forceinline__ void unit_fma_outer(const StageView &v, uint32_t ub, int wr, int lane,
-                                               float (&acc)[4 * RT][MT]) {
+template <class C, int RT, int MT, class V>
+__device__ __forceinline__ void unit_fma_outer(const V &v, int ul, int wr, int lane, float (&acc)[4 * RT][MT]) {
     const int rl = lane & 3, tl = lane >> 2;
 #pragma unroll 2
     for (int c = 0; c < 8; ++c) {
         float4 wv[4 * RT], xv[MT];
 #pragma unroll
-        for (int i = 0; i < 4 * RT; ++i) wv[i] = lds128(v.wrow(wr * RT * 16 + rl + 4 * i) + ub + c * 16);
+        for (int i = 0; i < 4 * RT; ++i) wv[i] = lds128(v.wa(wr * RT * 16 + rl + 4 * i, ul, c));
 #pragma unroll
-        for (int j = 0; j < MT; ++j) xv[j] = lds128(v.xrow(tl + 8 * j) + ub + c * 16);
+        for (int j = 0; j < MT; ++j) xv[j] = lds128(v.xa(tl + 8 * j, ul, c));
 #pragma unroll
         for (int i = 0; i < 4 * RT; ++i)
 #pragma unroll
@@ -245,14 +273,15 @@ __device__ __forceinline__ void unit_fma_outer(const StageView &v, uint32_t ub, 
     }
 }
 
-// Zero the bytes [valid, 128) of one k-unit in every loaded row (the tail of K).
-__device__ __forceinline__ void zero_unit_tail(const StageView &v, uint32_t ub, uint32_t valid, int lane) {
+// Zero the bytes [valid, 128) of one k-unit in every loaded row (the tail of K;
+// bulk layout only: the tensor layout is used only when K has no partial unit).
+__device__ __forceinline__ void zero_unit_tail(const StageView<false> &v, int ul, uint32_t valid, int lane) {
     const int chunks = static_cast<int>((128u - valid) >> 4);
     const int rows = v.rmax + 1 + v.tmax + 1;
     for (int idx = lane; idx < rows * chunks; idx += 32) {
         const int r = idx / chunks, c = idx - r * chunks;
-        const uint32_t base = (r <= v.rmax) ? v.wrow(r) : v.xrow(r - v.rmax - 1);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + ub + valid + c * 16), "r"(0u)
+        const uint32_t base = (r <= v.rmax) ? v.wa(r, ul, 0) : v.xa(r - v.rmax - 1, ul, 0);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + valid + c * 16), "r"(0u)
                      : "memory");
     }
     __syncwarp();
@@ -275,15 +304,18 @@ __device__ __forceinline__ void store_out(const StreamArgs &a, int n, int tok, f
 
 // ---- the kernel -------------------------------------------------------------
 
-template <int COMPUTE, int MT, int RT, int WR, int WK>
+template <int COMPUTE, int MT, int RT, int WR, int WK, bool TENSOR>
 __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 1)
-    hsp_stream_kernel(const __grid_constant__ StreamArgs a) {
+    hsp_stream_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                      const __grid_constant__ StreamArgs a) {
     using C = StreamCfg<COMPUTE, MT, RT, WR, WK>;
     constexpr int kSlots = C::kSlots, kXRows = C::kXRows;
 
-    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // The ring starts on a 1024-byte boundary (the swizzle pattern of the tensor
+    // layout repeats every 1024 bytes).
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + ((128u - (raw_addr & 127u)) & 127u);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t ring = smem_u32(smem);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.ring_bytes);
     uint64_t *empty = full + a.ring_stages;
@@ -297,15 +329,24 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     const int u_slice0 = slice * a.units_per_slice;
     const int u_slice1 = min(a.units_total, u_slice0 + a.units_per_slice);
     const int nst = max(0, (u_slice1 - u_slice0 + a.stage_units - 1) / a.stage_units);
+    const int npre = min(nst, a.ring_stages);
+    // The tensor layout has one producer thread (one arrival per phase); in the bulk
+    // layout every warp issues a share of each stage and arrives once.
+    constexpr uint32_t kFullCount = TENSOR ? 1u : static_cast<uint32_t>(C::kNW);
+    const bool producer = TENSOR && warp == C::kNCW && lane == 0;
 
     if (tid == 0) {
         for (int s = 0; s < a.ring_stages; ++s) {
-            mbar_init(smem_u32(&full[s]), C::kNW);
+            mbar_init(smem_u32(&full[s]), kFullCount);
             mbar_init(smem_u32(&empty[s]), C::kNCW);
             armed[s] = -1;
         }
         *abort_flag = 0;
         mbar_fence_init();
+    }
+    if (producer) {
+        tma_prefetch_map(&tmap_w);
+        tma_prefetch_map(&tmap_x);
     }
     __syncthreads();
     if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
@@ -322,11 +363,14 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
 #pragma unroll
     for (int i = 0; i < (int)(sizeof(acc_fo) / sizeof(float)); ++i) (&acc_fo[0][0])[i] = 0.f;
 
-    // ---------------- copy issue (every warp, lane-parallel) ----------------
+    const uint64_t w_policy = l2_policy_evict_first();
+    // every stage's box holds the same bytes (units past the tensor are zero-filled)
+    const uint32_t stage_tx = static_cast<uint32_t>((a.rows_per_cta + a.M) * a.stage_units * kUnitBytes);
+
+    // ---------------- bulk layout: copy issue by every warp, lane-parallel ----------------
     // Warp `warp` copies weight rows r = warp + 9 l and token rows t = warp + 9 l;
     // lane l issues the copy of its row, after lane 0 has raised the stage's
     // expected byte count by the warp's share.  Each warp arrives once per phase.
-    const uint64_t w_policy = l2_policy_evict_first();
     const char *wrow0 = a.w + static_cast<int64_t>(row0) * a.row_bytes;
     auto span = [&](int i, int64_t &byte0, uint32_t &nbytes) {
         const int u0 = u_slice0 + i * a.stage_units;
@@ -337,8 +381,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     };
     const int my_rows = rows_here > warp ? (rows_here - warp + C::kNW - 1) / C::kNW : 0;
     const int my_toks = a.M > warp ? (a.M - warp + C::kNW - 1) / C::kNW : 0;
-    // lane-parallel issue of this warp's rows (and tokens) of one stage; lanes past
-    // 32 loop (a CTA has at most 128 rows and 64 tokens)
+    // lanes past 32 loop (a CTA has at most 128 rows and 64 tokens)
     auto issue_w = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
         const uint32_t base = ring + slot * a.stage_bytes;
         for (int l = lane; l < my_rows; l += 32) {
@@ -347,46 +390,92 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         }
     };
     auto issue_x = [&](int slot, int64_t byte0, uint32_t nbytes, uint32_t fb) {
-        const uint32_t base = ring + slot * a.stage_bytes + a.rows_per_cta * a.pitch;
+        const uint32_t base = ring + slot * a.stage_bytes + a.x_off;
         for (int l = lane; l < my_toks; l += 32) {
             const int t = warp + C::kNW * l;
             bulk_load(base + t * a.pitch, a.x + t * a.row_bytes + byte0, nbytes, fb);
         }
     };
-    const int npre = min(nst, a.ring_stages);
+    // ---------------- tensor layout: one producer thread, two boxes per stage ----------------
+    auto tensor_w = [&](int i, int slot) {
+        tma_load_3d_hint(ring + slot * a.stage_bytes, &tmap_w, 0, row0, u_slice0 + i * a.stage_units,
+                         smem_u32(&full[slot]), w_policy);
+    };
+    auto tensor_x = [&](int i, int slot) {
+        tma_load_3d(ring + slot * a.stage_bytes + a.x_off, &tmap_x, 0, 0, u_slice0 + i * a.stage_units,
+                    smem_u32(&full[slot]));
+    };
+
     // Weights of the first ring's worth of stages: before the grid dependency.
-    for (int i = 0; i < npre; ++i) {
-        if (i == a.skip_stage) continue;
-        int64_t b0;
-        uint32_t nb;
-        span(i, b0, nb);
-        if (lane == 0 && my_rows > 0) mbar_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_rows) * nb);
+    if constexpr (TENSOR) {
+        if (producer) {
+            for (int i = 0; i < npre; ++i) {
+                if (i == a.skip_stage) continue;
+                mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx);
+                tensor_w(i, i);
+                armed[i] = i;
+            }
+        }
         __syncwarp();
-        issue_w(i, b0, nb, smem_u32(&full[i]));
+    } else {
+        for (int i = 0; i < npre; ++i) {
+            if (i == a.skip_stage) continue;
+            int64_t b0;
+            uint32_t nb;
+            span(i, b0, nb);
+            if (lane == 0 && my_rows > 0) mbar_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_rows) * nb);
+            __syncwarp();
+            issue_w(i, b0, nb, smem_u32(&full[i]));
+        }
     }
     // Weights of later kernels named by the caller: into L2, before the grid dependency.
     if (warp == C::kNCW && a.prefetch.count > 0)
         prefetch_ranges_l2(a.prefetch, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y, lane);
     // Activations are written by the previous kernel on the stream.
     griddep_wait();
-    for (int i = 0; i < npre; ++i) {
-        if (i == a.skip_stage) continue;
-        int64_t b0;
-        uint32_t nb;
-        span(i, b0, nb);
-        if (lane == 0) {
-            mbar_arrive_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_toks) * nb);
-            if (warp == 0) armed[i] = i;
+    if constexpr (TENSOR) {
+        if (producer)
+            for (int i = 0; i < npre; ++i)
+                if (i != a.skip_stage) tensor_x(i, i);
+    } else {
+        for (int i = 0; i < npre; ++i) {
+            if (i == a.skip_stage) continue;
+            int64_t b0;
+            uint32_t nb;
+            span(i, b0, nb);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(smem_u32(&full[i]), static_cast<uint32_t>(my_toks) * nb);
+                if (warp == 0) armed[i] = i;
+            }
+            __syncwarp();
+            issue_x(i, b0, nb, smem_u32(&full[i]));
         }
-        __syncwarp();
-        issue_x(i, b0, nb, smem_u32(&full[i]));
     }
     __syncwarp();
 
-    // ---------------- consume stage i, then refill its slot with stage i + ring ----------------
     const int wk = warp % WK, wr = warp / WK;
     const bool consumer = warp < C::kNCW;
     const bool has_rows = consumer && wr * RT * 16 < rows_here;
+    if constexpr (TENSOR) {
+        // ---------------- tensor layout: the producer refills released slots ----------------
+        if (producer) {
+            for (int j = npre; j < nst; ++j) {
+                const int slot = j % a.ring_stages;
+                const uint32_t par = static_cast<uint32_t>((j / a.ring_stages) - 1) & 1u;
+                if (!thread_wait(smem_u32(&empty[slot]), par, a.wait_limit_ns, abort_flag)) {
+                    record_timeout(a.err_word, abort_flag);
+                    break;
+                }
+                if (j == a.skip_stage) continue;
+                mbar_arrive_expect_tx(smem_u32(&full[slot]), stage_tx);
+                tensor_w(j, slot);
+                tensor_x(j, slot);
+                armed[slot] = j;
+            }
+        }
+        __syncwarp();  // the producer's warp reconverges before the barriers below
+    }
+    // ---------------- consume stage i (bulk layout: then refill its slot with stage i + ring) ----------------
     for (int i = 0; i < nst; ++i) {
         const int slot = i % a.ring_stages;
         const uint32_t par = static_cast<uint32_t>(i / a.ring_stages) & 1u;
@@ -397,57 +486,66 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             }
             const int u0 = u_slice0 + i * a.stage_units;
             const int u1 = min(u0 + a.stage_units, u_slice1);
-            StageView v;
+            StageView<TENSOR> v;
             v.w = ring + slot * a.stage_bytes;
-            v.x = v.w + a.rows_per_cta * a.pitch;
-            v.pitch = a.pitch;
+            v.x = v.w + a.x_off;
+            if constexpr (TENSOR) {
+                v.wrows = a.rows_per_cta;
+                v.xrows = a.M;
+            } else {
+                v.pitch = a.pitch;
+            }
             v.rmax = rows_here - 1;
             v.tmax = a.M - 1;
             bool zeroed = false;
             // units of this warp: u = u0 + j with u mod WK == wk, in increasing order
             for (int u = u0 + ((wk - u0 % WK) % WK + WK) % WK; u < u1; u += WK) {
-                const uint32_t ub = static_cast<uint32_t>(u - u0) * kUnitBytes;
-                const int64_t valid = a.row_bytes - static_cast<int64_t>(u) * kUnitBytes;
-                if (valid < kUnitBytes) {
-                    zero_unit_tail(v, ub, static_cast<uint32_t>(valid), lane);
-                    zeroed = true;
+                const int ul = u - u0;
+                if constexpr (!TENSOR) {
+                    const int64_t valid = a.row_bytes - static_cast<int64_t>(u) * kUnitBytes;
+                    if (valid < kUnitBytes) {
+                        zero_unit_tail(v, ul, static_cast<uint32_t>(valid), lane);
+                        zeroed = true;
+                    }
                 }
                 if (!has_rows) continue;
                 if constexpr (COMPUTE == kFmaBf16) {
-                    unit_fma_ksplit<C, RT, 2>(v, ub, wr, lane, a.M, acc_fk);
+                    unit_fma_ksplit<C, RT, 2>(v, ul, wr, lane, a.M, acc_fk);
                 } else if constexpr (COMPUTE == kFmaFp32) {
                     if constexpr (MT == 1)
-                        unit_fma_ksplit<C, RT, 8>(v, ub, wr, lane, a.M, acc_fk);
+                        unit_fma_ksplit<C, RT, 8>(v, ul, wr, lane, a.M, acc_fk);
                     else
-                        unit_fma_outer<C, RT, MT>(v, ub, wr, lane, acc_fo);
+                        unit_fma_outer<C, RT, MT>(v, ul, wr, lane, acc_fo);
                 } else {
-                    unit_mma<C, RT, MT, kChains>(v, ub, wr, lane, acc_mma);
+                    unit_mma<C, RT, MT, kChains>(v, ul, wr, lane, acc_mma);
                 }
             }
             if (zeroed) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
         }
-        const int j = i + a.ring_stages;
-        if (j < nst) {
-            // every consumer has released the slot: issue this warp's share of stage j
-            if (!warp_wait(smem_u32(&empty[slot]), par, a.wait_limit_ns, abort_flag)) {
-                if (lane == 0) record_timeout(a.err_word, abort_flag);
-                break;
-            }
-            if (j != a.skip_stage) {
-                int64_t b0;
-                uint32_t nb;
-                span(j, b0, nb);
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(smem_u32(&full[slot]), static_cast<uint32_t>(my_rows + my_toks) * nb);
-                    if (warp == 0) armed[slot] = j;
+        if constexpr (!TENSOR) {
+            const int j = i + a.ring_stages;
+            if (j < nst) {
+                // every consumer has released the slot: issue this warp's share of stage j
+                if (!warp_wait(smem_u32(&empty[slot]), par, a.wait_limit_ns, abort_flag)) {
+                    if (lane == 0) record_timeout(a.err_word, abort_flag);
+                    break;
+                }
+                if (j != a.skip_stage) {
+                    int64_t b0;
+                    uint32_t nb;
+                    span(j, b0, nb);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(smem_u32(&full[slot]), static_cast<uint32_t>(my_rows + my_toks) * nb);
+                        if (warp == 0) armed[slot] = j;
+                    }
+                    __syncwarp();
+                    issue_w(slot, b0, nb, smem_u32(&full[slot]));
+                    issue_x(slot, b0, nb, smem_u32(&full[slot]));
                 }
                 __syncwarp();
-                issue_w(slot, b0, nb, smem_u32(&full[slot]));
-                issue_x(slot, b0, nb, smem_u32(&full[slot]));
             }
-            __syncwarp();
         }
     }
 

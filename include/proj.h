@@ -126,8 +126,11 @@ typedef struct {
     int32_t stages_total;  /* ring stages of one K slice */
     int32_t threads;       /* threads per CTA (consumer warps + 1 producer warp) */
     int32_t units_per_slice; /* 128-byte k-units per K slice (fixes the summation order with k_warps) */
-    int32_t engine;          /* 0 bulk-copy + mma.sync / FMA kernel, 1 tensor-memory (tcgen05) kernel */
-    int32_t reserved[3];
+    int32_t engine;          /* 0 streaming mma.sync / FMA kernel, 1 tensor-memory (tcgen05) kernel */
+    int32_t tensor_copies;   /* streaming kernel: 1 = one 3-D tensor copy per stage for the weights
+                              * and one for the tokens (rows a multiple of 128 bytes), 0 = one 1-D
+                              * bulk copy per row and stage (any other K) */
+    int32_t reserved[2];
 } proj_plan_info;
 
 /*

@@ -16,6 +16,13 @@ are real checkpoints that are not available here, so every value is drawn):
                 Walkthrough: q_a 1536 ++ kv_a 576 ++ indexer wk 128 ++ weights_proj 64.
   glm_fused_a   TensorRT-LLM PR #20502 (GLM-5.2 decode target), glmFusedAGemm
                 commit message: hidden 6144, q_a 2048 ++ kv_a 576 ++ indexer wk 128.
+  glm_fused_a_2784
+                the same commit message's wider cell: 2624 rows (q_a 2048,
+                compressed KV 512, k_pe 64) plus the indexer's wk 128 and
+                weights_proj 32 rows appended to the same weight, up to 8 tokens.
+  glm_router_fp32
+                the same page, glmRouterGemm commit message: FP32 router logits of
+                256 experts at hidden 6144 for 1 to 16 tokens.
 
 Recipe: X ~ N(0, 1) and W ~ N(0, 0.02), drawn in fp32 with a CPU
 torch.Generator and rounded once to bf16 (torch's round-to-nearest-even) when
@@ -70,6 +77,9 @@ WORKLOADS = {
                            ("q_a", "kv_a", "idx_wk", "idx_wp"), BF16, (1, 8, 32, 64)),
     "glm_fused_a": Workload(5, "glm_fused_a", 6144, (2048, 576, 128),
                             ("q_a", "kv_a", "idx_wk"), BF16, tuple(range(1, 9))),
+    "glm_fused_a_2784": Workload(6, "glm_fused_a_2784", 6144, (2048, 512, 64, 128, 32),
+                                 ("q_a", "compressed_kv", "k_pe", "idx_wk", "idx_wp"), BF16, (1, 4, 8)),
+    "glm_router_fp32": Workload(7, "glm_router_fp32", 6144, (256,), ("router",), FP32, (1, 4, 16)),
 }
 
 
