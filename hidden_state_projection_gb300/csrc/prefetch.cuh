@@ -4,7 +4,9 @@
 // before the grid-dependency wait each CTA prefetches up to four caller tensors --
 // weights that later kernels of the step read -- into L2 in 16 KB bulk prefetches
 // spread over the CTAs.  Here chunk c of the concatenated ranges goes to CTA
-// (c mod CTAs), lane-parallel inside the calling warp.
+// (c mod CTAs), lane-parallel inside the calling warp.  The streaming kernel issues
+// them after its own weight and token copies (measured: ahead of the token copies
+// they delay the first stage), the tensor-memory kernel before its grid wait.
 #pragma once
 
 #include <stdint.h>

@@ -428,9 +428,6 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             issue_w(i, b0, nb, smem_u32(&full[i]));
         }
     }
-    // Weights of later kernels named by the caller: into L2, before the grid dependency.
-    if (warp == C::kNCW && a.prefetch.count > 0)
-        prefetch_ranges_l2(a.prefetch, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y, lane);
     // Activations are written by the previous kernel on the stream.
     griddep_wait();
     if constexpr (TENSOR) {
@@ -452,6 +449,11 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         }
     }
     __syncwarp();
+    // Weights of later kernels named by the caller: into L2, after this CTA's own
+    // copies (the copy engine serves requests in order; prefetches queued ahead of
+    // the token copies would hold up the first stage).
+    if (warp == C::kNCW && a.prefetch.count > 0)
+        prefetch_ranges_l2(a.prefetch, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y, lane);
 
     const int wk = warp % WK, wr = warp / WK;
     const bool consumer = warp < C::kNCW;

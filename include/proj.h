@@ -157,9 +157,10 @@ proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_s
  * PROJ_MAX_PREFETCH caller-named global ranges into L2 (TensorRT-LLM PR #20502,
  * glmFusedAGemm commit message: before the grid-dependency wait each CTA prefetches
  * up to four caller tensors -- weights that later kernels of the step read -- into
- * L2 in 16 KB bulk prefetches spread over the CTAs).  The ranges are only read as
- * a hint: the outputs are bitwise those of proj_fused_gemm.  Ranges must stay
- * allocated until the call has completed on the stream.
+ * L2 in 16 KB bulk prefetches spread over the CTAs; here the streaming kernel
+ * issues them right after its own copies).  The ranges are only read as a hint:
+ * the outputs are bitwise those of proj_fused_gemm.  Ranges must stay allocated
+ * until the call has completed on the stream.
  */
 proj_status proj_fused_gemm_prefetch(const void *x, const void *w_cat, const int32_t *n_splits,
                                      int32_t num_splits, void *const *outs, int32_t M, int32_t K,
