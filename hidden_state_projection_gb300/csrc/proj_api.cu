@@ -421,7 +421,15 @@ proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0,
 
 // ---- tensor-memory plan ----------------------------------------------------
 
-bool use_umma(int M, proj_dtype dt) { return M > 8 && dt == PROJ_BF16 && g_opt_large_m_path.load() == 0; }
+// bf16 with 9 <= M <= 64: the streaming kernel up to kStreamMaxM tokens, the
+// tensor-memory kernel above (measured on GB300, qk_indexer: M = 16 10.96 vs 12.13 us,
+// M = 32 17.8 vs 12.3 us); option large_m_path 1 / 2 forces one of them.
+constexpr int kStreamMaxM = 16;
+bool use_umma(int M, proj_dtype dt) {
+    if (M <= 8 || dt != PROJ_BF16) return false;
+    const int o = g_opt_large_m_path.load();
+    return o == 2 || (o == 0 && M > kStreamMaxM);
+}
 
 struct UPlan {
     proj_plan_info info;
@@ -768,9 +776,10 @@ proj_status proj_set_options(const proj_options *opt) {
     if (opt->pdl < -1 || opt->pdl > 1) return fail(PROJ_ERR_INVALID_ARG, "pdl must be -1, 0 or 1");
     if (opt->wait_limit_us < 0 || opt->skip_stage_plus1 < 0)
         return fail(PROJ_ERR_INVALID_ARG, "wait_limit_us and skip_stage_plus1 must be >= 0");
-    if (opt->large_m_path < 0 || opt->large_m_path > 1 || opt->l2_prefetch < 0 || opt->l2_prefetch > 1 ||
+    if (opt->large_m_path < 0 || opt->large_m_path > 2 || opt->l2_prefetch < 0 || opt->l2_prefetch > 1 ||
         opt->trigger_early < 0 || opt->trigger_early > 1 || opt->small_m_path < 0 || opt->small_m_path > 1)
-        return fail(PROJ_ERR_INVALID_ARG, "large_m_path, small_m_path, l2_prefetch and trigger_early must be 0 or 1");
+        return fail(PROJ_ERR_INVALID_ARG,
+                    "large_m_path must be 0, 1 or 2; small_m_path, l2_prefetch and trigger_early 0 or 1");
     if (opt->pdl >= 0) g_opt_pdl.store(opt->pdl);
     g_opt_wait_us.store(opt->wait_limit_us);
     g_opt_skip_stage_plus1.store(opt->skip_stage_plus1);

@@ -1,0 +1,43 @@
+// scatter.cuh -- the split-output epilogue shared by both kernels.
+//
+// TensorRT-LLM PR #20636, Description: one GEMM over the row-concatenated weight,
+// its halves returned as dense [M, N_i] outputs.  Row n of a launch belongs to split
+// i with off[i] <= n < off[i] + rows[i]; its value for token t goes to
+// out[i][t * rows[i] + (n - off[i])], rounded once to the output type.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "stream_args.h"
+
+namespace hsp {
+
+// Where one output row lives: its element for token t is at base + t * stride.
+struct OutRow {
+    char *base;
+    int64_t stride_bytes;
+};
+
+template <bool BF16_OUT>
+__device__ __forceinline__ OutRow out_row(const SplitTable &s, int n) {
+    int i = 0;
+#pragma unroll 1
+    while (i + 1 < s.count && n >= s.off[i + 1]) ++i;
+    constexpr int esz = BF16_OUT ? 2 : 4;
+    OutRow o;
+    o.base = static_cast<char *>(s.out[i]) + static_cast<int64_t>(n - s.off[i]) * esz;
+    o.stride_bytes = static_cast<int64_t>(s.rows[i]) * esz;
+    return o;
+}
+
+template <bool BF16_OUT>
+__device__ __forceinline__ void store_tok(const OutRow &o, int tok, float v) {
+    char *p = o.base + static_cast<int64_t>(tok) * o.stride_bytes;
+    if constexpr (BF16_OUT)
+        *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
+    else
+        *reinterpret_cast<float *>(p) = v;
+}
+
+}  // namespace hsp

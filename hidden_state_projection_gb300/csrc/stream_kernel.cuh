@@ -57,6 +57,7 @@
 
 #include "prefetch.cuh"
 #include "ptx.cuh"
+#include "scatter.cuh"
 #include "stream_args.h"
 
 namespace hsp {
@@ -287,21 +288,6 @@ __device__ __forceinline__ void zero_unit_tail(const StageView<false> &v, int ul
     __syncwarp();
 }
 
-// ---- output scatter -------------------------------------------------------
-
-template <int COMPUTE>
-__device__ __forceinline__ void store_out(const StreamArgs &a, int n, int tok, float v) {
-    int i = 0;
-#pragma unroll 1
-    while (i + 1 < a.splits.count && n >= a.splits.off[i + 1]) ++i;
-    const int64_t idx = static_cast<int64_t>(tok) * a.splits.rows[i] + (n - a.splits.off[i]);
-    if constexpr (COMPUTE == kMmaBf16 || COMPUTE == kFmaBf16) {
-        static_cast<__nv_bfloat16 *>(a.splits.out[i])[idx] = __float2bfloat16_rn(v);
-    } else {
-        static_cast<float *>(a.splits.out[i])[idx] = v;
-    }
-}
-
 // ---- the kernel -------------------------------------------------------------
 
 template <int COMPUTE, int MT, int RT, int WR, int WK, bool TENSOR>
@@ -335,7 +321,21 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     constexpr uint32_t kFullCount = TENSOR ? 1u : static_cast<uint32_t>(C::kNW);
     const bool producer = TENSOR && warp == C::kNCW && lane == 0;
 
-    if (tid == 0) {
+    const uint64_t w_policy = l2_policy_evict_first();
+    // every stage's box holds the same bytes (units past the tensor are zero-filled)
+    const uint32_t stage_tx = static_cast<uint32_t>((a.rows_per_cta + a.M) * a.stage_units * kUnitBytes);
+    // ---------------- tensor layout: one producer thread, two boxes per stage ----------------
+    auto tensor_w = [&](int i, int slot) {
+        tma_load_3d_hint(ring + slot * a.stage_bytes, &tmap_w, 0, row0, u_slice0 + i * a.stage_units,
+                         smem_u32(&full[slot]), w_policy);
+    };
+    auto tensor_x = [&](int i, int slot) {
+        tma_load_3d(ring + slot * a.stage_bytes + a.x_off, &tmap_x, 0, 0, u_slice0 + i * a.stage_units,
+                    smem_u32(&full[slot]));
+    };
+
+    // The barriers are initialised by the producer (tensor layout) or by thread 0.
+    if (TENSOR ? producer : tid == 0) {
         for (int s = 0; s < a.ring_stages; ++s) {
             mbar_init(smem_u32(&full[s]), kFullCount);
             mbar_init(smem_u32(&empty[s]), C::kNCW);
@@ -343,10 +343,18 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         }
         *abort_flag = 0;
         mbar_fence_init();
-    }
-    if (producer) {
-        tma_prefetch_map(&tmap_w);
-        tma_prefetch_map(&tmap_x);
+        if constexpr (TENSOR) {
+            // Weights of the first ring's worth of stages: before the grid dependency,
+            // and before the CTA barrier (they need nothing but the barriers above).
+            tma_prefetch_map(&tmap_w);
+            tma_prefetch_map(&tmap_x);
+            for (int i = 0; i < npre; ++i) {
+                if (i == a.skip_stage) continue;
+                mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx);
+                tensor_w(i, i);
+                armed[i] = i;
+            }
+        }
     }
     __syncthreads();
     if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
@@ -362,10 +370,6 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     for (int i = 0; i < (int)(sizeof(acc_fk) / sizeof(float)); ++i) (&acc_fk[0][0])[i] = 0.f;
 #pragma unroll
     for (int i = 0; i < (int)(sizeof(acc_fo) / sizeof(float)); ++i) (&acc_fo[0][0])[i] = 0.f;
-
-    const uint64_t w_policy = l2_policy_evict_first();
-    // every stage's box holds the same bytes (units past the tensor are zero-filled)
-    const uint32_t stage_tx = static_cast<uint32_t>((a.rows_per_cta + a.M) * a.stage_units * kUnitBytes);
 
     // ---------------- bulk layout: copy issue by every warp, lane-parallel ----------------
     // Warp `warp` copies weight rows r = warp + 9 l and token rows t = warp + 9 l;
@@ -396,28 +400,8 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             bulk_load(base + t * a.pitch, a.x + t * a.row_bytes + byte0, nbytes, fb);
         }
     };
-    // ---------------- tensor layout: one producer thread, two boxes per stage ----------------
-    auto tensor_w = [&](int i, int slot) {
-        tma_load_3d_hint(ring + slot * a.stage_bytes, &tmap_w, 0, row0, u_slice0 + i * a.stage_units,
-                         smem_u32(&full[slot]), w_policy);
-    };
-    auto tensor_x = [&](int i, int slot) {
-        tma_load_3d(ring + slot * a.stage_bytes + a.x_off, &tmap_x, 0, 0, u_slice0 + i * a.stage_units,
-                    smem_u32(&full[slot]));
-    };
-
-    // Weights of the first ring's worth of stages: before the grid dependency.
-    if constexpr (TENSOR) {
-        if (producer) {
-            for (int i = 0; i < npre; ++i) {
-                if (i == a.skip_stage) continue;
-                mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx);
-                tensor_w(i, i);
-                armed[i] = i;
-            }
-        }
-        __syncwarp();
-    } else {
+    // Weights of the first ring's worth of stages (bulk layout): before the grid dependency.
+    if constexpr (!TENSOR) {
         for (int i = 0; i < npre; ++i) {
             if (i == a.skip_stage) continue;
             int64_t b0;
@@ -623,6 +607,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     griddep_wait();
 
     // ---- warp partials added in warp order; single-slice CTAs store here ----
+    constexpr bool kBf16Out = (COMPUTE == kMmaBf16 || COMPUTE == kFmaBf16);
     bool stored = false;
     if (!aborted) {
         for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
@@ -632,7 +617,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
 #pragma unroll
             for (int q = 1; q < WK; ++q) v += red[(q * kSlots + slot) * kXRows + tok];
             if (a.slices == 1) {
-                store_out<COMPUTE>(a, row0 + slot, tok, v);
+                store_tok<kBf16Out>(out_row<kBf16Out>(a.splits, row0 + slot), tok, v);
                 stored = true;
             } else {
                 red[slot * kXRows + tok] = v;
@@ -669,7 +654,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 if (tok >= a.M || slot >= rows_here) continue;
                 float v = recv[rr * kXRows + tok];
                 for (int q = 1; q < a.slices; ++q) v += recv[(q * per + rr) * kXRows + tok];
-                store_out<COMPUTE>(a, row0 + slot, tok, v);
+                store_tok<kBf16Out>(out_row<kBf16Out>(a.splits, row0 + slot), tok, v);
                 stored = true;
             }
         }

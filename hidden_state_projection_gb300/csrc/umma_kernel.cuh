@@ -38,6 +38,7 @@
 
 #include "prefetch.cuh"
 #include "ptx.cuh"
+#include "scatter.cuh"
 #include "stream_args.h"
 
 namespace hsp {
@@ -57,18 +58,6 @@ __device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, uint64_
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 7u) == 7u && ((*abort_flag != 0) || (global_timer_ns() - t0 > limit_ns))) return false;
     }
-}
-
-template <int COMPUTE>
-__device__ __forceinline__ void umma_store(const UmmaArgs &a, int n, int tok, float v) {
-    int i = 0;
-#pragma unroll 1
-    while (i + 1 < a.splits.count && n >= a.splits.off[i + 1]) ++i;
-    const int64_t idx = static_cast<int64_t>(tok) * a.splits.rows[i] + (n - a.splits.off[i]);
-    if constexpr (COMPUTE == kMmaBf16)
-        static_cast<__nv_bfloat16 *>(a.splits.out[i])[idx] = __float2bfloat16_rn(v);
-    else
-        static_cast<float *>(a.splits.out[i])[idx] = v;
 }
 
 template <int COMPUTE, int NT>
@@ -114,6 +103,16 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         *abort_flag = 0;
         *issued = 0;
         mbar_fence_init();
+        // The producer's first weight boxes go out before the CTA barrier and the TMEM
+        // allocation: they depend on nothing but the barriers initialised just above.
+        tma_prefetch_map(&tmap_w);
+        tma_prefetch_map(&tmap_x);
+        for (int i = 0; i < min(nkb, a.ring_stages); ++i) {
+            if (i == a.skip_stage) continue;
+            const uint32_t fb = smem_u32(&full[i]);
+            mbar_expect_tx(fb, kWBoxBytes);
+            tma_load_2d(ring + i * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb);
+        }
     }
     if (warp == 2) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -142,16 +141,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         prefetch_ranges_l2(a.prefetch, blockIdx.y * gridDim.x + blockIdx.x, gridDim.x * gridDim.y, lane);
 
     if (warp == 0 && lane == 0) {
-        // ---------------- copy producer ----------------
-        tma_prefetch_map(&tmap_w);
-        tma_prefetch_map(&tmap_x);
+        // ---------------- copy producer (its first weight boxes are already out) ----------------
         const int npre = min(nkb, a.ring_stages);
-        for (int i = 0; i < npre; ++i) {
-            if (i == a.skip_stage) continue;
-            const uint32_t fb = smem_u32(&full[i]);
-            mbar_expect_tx(fb, kWBoxBytes);
-            tma_load_2d(ring + i * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb);
-        }
         griddep_wait();
         for (int i = 0; i < npre; ++i) {
             if (i == a.skip_stage) continue;
@@ -252,11 +243,13 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     griddep_wait();  // outputs may still be read by the previous kernel on the stream
     bool stored = false;
+    constexpr bool kBf16Out = (COMPUTE == kMmaBf16);
     if (a.slices == 1) {
         if (!aborted && r < rows_here) {
+            const OutRow o = out_row<kBf16Out>(a.splits, row0 + r);
 #pragma unroll
             for (int t = 0; t < NT; ++t)
-                if (t < a.M) umma_store<COMPUTE>(a, row0 + r, t, v[t]);
+                if (t < a.M) store_tok<kBf16Out>(o, t, v[t]);
             stored = true;
         }
     } else {
@@ -308,10 +301,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                         acc.z += part[q].z;
                         acc.w += part[q].w;
                     }
-                const float o[4] = {acc.x, acc.y, acc.z, acc.w};
+                const float o4[4] = {acc.x, acc.y, acc.z, acc.w};
+                const OutRow o = out_row<kBf16Out>(a.splits, row0 + row);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (t4 + j < a.M) umma_store<COMPUTE>(a, row0 + row, t4 + j, o[j]);
+                    if (t4 + j < a.M) store_tok<kBf16Out>(o, t4 + j, o4[j]);
                 stored = true;
             }
         }

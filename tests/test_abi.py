@@ -143,6 +143,13 @@ def test_pack_check_and_options(hsp):
                                  "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0, "small_m_path": 0}
     with pytest.raises(hsp.ProjError):
         hsp.set_options(wait_limit_us=-1)
+    with pytest.raises(hsp.ProjError):
+        hsp.set_options(large_m_path=3)
+    # the default engine for bf16: streaming up to 16 tokens, tensor memory above
+    assert [hsp.describe_plan(M, 7168, 2304, 0)["engine"] for M in (1, 8, 9, 16, 17, 64)] == [0, 0, 0, 0, 1, 1]
+    hsp.set_options(large_m_path=2)
+    assert [hsp.describe_plan(M, 7168, 2304, 0)["engine"] for M in (8, 9, 16, 17)] == [0, 1, 1, 1]
+    hsp.set_options(pdl=True)
 
 
 def test_prefetch_entry_validation(hsp):
