@@ -74,6 +74,10 @@ def _load():
     lib.oracle_accumulate.restype = None
     lib.oracle_round.argtypes = [vp, i64, ctypes.c_int, vp]
     lib.oracle_round.restype = None
+    lib.oracle_fused_rmsnorm.argtypes = [vp, vp, ctypes.POINTER(i32), i32, ctypes.POINTER(i32),
+                                         ctypes.POINTER(vp), ctypes.c_double, ctypes.POINTER(vp), i64, i64,
+                                         ctypes.c_int]
+    lib.oracle_fused_rmsnorm.restype = ctypes.c_int
     lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
     lib.oracle_double_to_bf16.restype = ctypes.c_uint16
     _lib = lib
@@ -141,6 +145,30 @@ def fused(x, w_cat, n_splits: Sequence[int], dtype: int, threads: int = 1):
 def separate(x, w_cat, n_splits: Sequence[int], dtype: int, threads: int = 1):
     """One projection per split over its row range of w_cat."""
     return _run("oracle_separate", x, w_cat, n_splits, dtype, threads)
+
+
+def fused_rmsnorm(x, w_cat, n_splits: Sequence[int], norm_cols: Sequence[int], gammas, eps: float, dtype: int):
+    """Fused projection with the RMSNorm epilogue: split i's first norm_cols[i] columns
+    are normalized per token and scaled by gammas[i] (an array of the data type, or
+    None when norm_cols[i] is 0)."""
+    lib = _load()
+    x = _in_array(x, dtype)
+    w_cat = _in_array(w_cat, dtype)
+    M, K = x.shape
+    if w_cat.shape != (sum(n_splits), K):
+        raise ValueError("w_cat shape does not match the splits")
+    odt = np.uint16 if dtype == BF16 else np.float32
+    outs = [np.empty((M, int(n)), dtype=odt) for n in n_splits]
+    gs = [None if g is None else _in_array(np.asarray(g), dtype) for g in gammas]
+    ns = (ctypes.c_int32 * len(n_splits))(*[int(n) for n in n_splits])
+    nc = (ctypes.c_int32 * len(n_splits))(*[int(c) for c in norm_cols])
+    gp = (ctypes.c_void_p * len(n_splits))(*[None if g is None else g.ctypes.data for g in gs])
+    ptrs = (ctypes.c_void_p * len(outs))(*[o.ctypes.data for o in outs])
+    rc = lib.oracle_fused_rmsnorm(x.ctypes.data, w_cat.ctypes.data, ns, len(n_splits), nc, gp, float(eps),
+                                  ptrs, M, K, dtype)
+    if rc != 0:
+        raise RuntimeError(f"oracle_fused_rmsnorm failed ({rc})")
+    return outs
 
 
 def cpu_count() -> int:

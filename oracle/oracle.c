@@ -40,6 +40,18 @@
  *
  * Threads split the output rows n; each y[m][n] is computed by one thread with
  * the same loop, so the result does not depend on the thread count.
+ *
+ * RMSNorm epilogue (oracle_fused_rmsnorm): the consumers of the q_a / kv_a
+ * projections are RMSNorms (TensorRT-LLM PR #20636, Description: "the q_norm /
+ * kv_norm RMSNorms"; PR #20502, glm_mla_kv_half_append commit message: RMSNorm of
+ * the 512 latent columns of the raw kv_a_proj output).  For a split i with
+ * c_i = norm_cols[i] > 0 and every token m, from the fp64 sums above:
+ *
+ *   ms[m]  = (1 / c_i) * sum_{r < c_i} y[m][off_i + r]^2          (fp64, increasing r)
+ *   out_i[m][r] = round_out( y[m][off_i + r] / sqrt(ms[m] + eps) * gamma_i[r] )  r < c_i
+ *   out_i[m][r] = round_out( y[m][off_i + r] )                                   r >= c_i
+ *
+ * with gamma_i in the data type; one rounding per output, as for the projection.
  */
 #include <math.h>
 #include <pthread.h>
@@ -210,5 +222,49 @@ int oracle_separate(const void *x, const void *w_cat, const int32_t *n_splits, i
         if (rc) return rc;
         off += n_splits[i];
     }
+    return 0;
+}
+
+/* The fused projection followed by the RMSNorm epilogue described at the top.
+ * norm_cols[i] in [0, n_splits[i]] (0: split i is not normalized); gammas[i]
+ * points to norm_cols[i] elements of the data type (unused when norm_cols[i] is 0).
+ * Returns 0 on success, -1 on bad arguments or allocation failure. */
+int oracle_fused_rmsnorm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                         const int32_t *norm_cols, const void *const *gammas, double eps,
+                         void *const *outs, int64_t M, int64_t K, int dtype) {
+    if (M < 0 || K < 0 || num_splits < 1 || !n_splits || !outs || !norm_cols || !gammas) return -1;
+    int64_t N = 0;
+    for (int32_t i = 0; i < num_splits; ++i) {
+        if (n_splits[i] < 0 || norm_cols[i] < 0 || norm_cols[i] > n_splits[i]) return -1;
+        if (norm_cols[i] > 0 && !gammas[i]) return -1;
+        N += n_splits[i];
+    }
+    if (M == 0 || N == 0) return 0;
+    double *y = (double *)malloc(sizeof(double) * (size_t)(M * N));
+    if (!y) return -1;
+    accumulate_rows(x, w_cat, M, K, dtype, 0, N, y, N);
+    int64_t off = 0;
+    for (int32_t i = 0; i < num_splits; ++i) {
+        const int64_t ni = n_splits[i], ci = norm_cols[i];
+        for (int64_t m = 0; m < M; ++m) {
+            double inv = 1.0;
+            if (ci > 0) {
+                double ss = 0.0;
+                for (int64_t r = 0; r < ci; ++r) {
+                    const double v = y[m * N + off + r];
+                    ss += v * v;
+                }
+                inv = 1.0 / sqrt(ss / (double)ci + eps);
+            }
+            for (int64_t r = 0; r < ni; ++r) {
+                double v = y[m * N + off + r];
+                if (r < ci) v = v * inv * load_elem(gammas[i], r, dtype);
+                if (dtype == ORACLE_BF16) ((uint16_t *)outs[i])[m * ni + r] = oracle_double_to_bf16(v);
+                else ((float *)outs[i])[m * ni + r] = (float)v;
+            }
+        }
+        off += ni;
+    }
+    free(y);
     return 0;
 }

@@ -284,3 +284,75 @@ def test_pins_reject_planted_mistakes(oracle_mod):
     good = np.concatenate([o.astype(np.float64) for o in
                            oracle_mod.fused(_bits(x), _bits(torch.cat(ws, 0)), (3, 5), oracle_mod.FP32)], 1)
     assert np.array_equal(good, exact)
+
+
+# ---------------------------------------------------------------- RMSNorm epilogue
+
+def _f32(a):
+    return np.asarray(a, dtype=np.float32)
+
+
+def test_rmsnorm_golden_closed_forms(oracle_mod):
+    with open(os.path.join(GOLDEN, "rmsnorm_closed_forms.json")) as f:
+        spec = json.load(f)
+    x = _f32([[1.0, 1.0]])
+    w = _f32([[3.0, 0.0], [0.0, 4.0]])
+    for case in spec["cases"]:
+        (out,) = oracle_mod.fused_rmsnorm(x, w, (2,), (2,), [_f32(case["gamma"])], case["eps"], oracle_mod.FP32)
+        if "expect_sqrt2_times" in case:
+            exact = [c * np.sqrt(np.float64(2.0)) for c in case["expect_sqrt2_times"]]
+        else:
+            exact = [c / np.sqrt(np.float64(13.0)) for c in case["expect_over_sqrt13"]]
+        assert np.array_equal(out[0], _f32(exact)), (case["name"], out[0], exact)
+
+
+def test_rmsnorm_unit_mean_square(oracle_mod):
+    """gamma = 1, eps = 0: every token's normalized columns have mean square 1."""
+    x, ws = W.random_case(512, (96, 40), 3, "fp32", seed=31)
+    wcat = torch.cat(ws, 0)
+    g = [np.ones(96, np.float32), np.ones(24, np.float32)]
+    a, b = oracle_mod.fused_rmsnorm(_bits(x), _bits(wcat), (96, 40), (96, 24), g, 0.0, oracle_mod.FP32)
+    for out, c in ((a, 96), (b, 24)):
+        ms = np.mean(out[:, :c].astype(np.float64) ** 2, axis=1)
+        assert np.allclose(ms, 1.0, rtol=0, atol=1e-6), ms
+
+
+def test_rmsnorm_scale_invariance_and_gamma_linearity(oracle_mod):
+    """eps = 0: doubling x leaves the normalized columns unchanged bit for bit and
+    doubles the others; doubling gamma doubles the normalized columns."""
+    x, ws = W.random_case(256, (48, 20), 2, "bf16", seed=32)
+    wcat = torch.cat(ws, 0)
+    gam = torch.randn(48, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    g1 = [_bits(gam), None]
+    g2 = [_bits(gam * 2), None]
+    base = oracle_mod.fused_rmsnorm(_bits(x), _bits(wcat), (48, 20), (48, 0), g1, 0.0, oracle_mod.BF16)
+    twice_x = oracle_mod.fused_rmsnorm(_bits(x * 2), _bits(wcat), (48, 20), (48, 0), g1, 0.0, oracle_mod.BF16)
+    twice_g = oracle_mod.fused_rmsnorm(_bits(x), _bits(wcat), (48, 20), (48, 0), g2, 0.0, oracle_mod.BF16)
+    assert np.array_equal(base[0], twice_x[0])
+    assert np.array_equal(_bf16_bits_to_float(twice_x[1]), 2 * _bf16_bits_to_float(base[1]))
+    assert np.array_equal(_bf16_bits_to_float(twice_g[0]), 2 * _bf16_bits_to_float(base[0]))
+
+
+def test_rmsnorm_leaves_other_columns_as_the_projection(oracle_mod):
+    """Columns past norm_cols, and splits with norm_cols 0, are the plain projection."""
+    x, ws = W.random_case(576, (64, 36, 16), 4, "bf16", seed=33)
+    wcat = torch.cat(ws, 0)
+    gam = [_bits(torch.ones(64, dtype=torch.bfloat16)), _bits(torch.ones(32, dtype=torch.bfloat16)), None]
+    normed = oracle_mod.fused_rmsnorm(_bits(x), _bits(wcat), (64, 36, 16), (64, 32, 0), gam, 1e-6, oracle_mod.BF16)
+    plain = oracle_mod.fused(_bits(x), _bits(wcat), (64, 36, 16), oracle_mod.BF16)
+    assert np.array_equal(normed[1][:, 32:], plain[1][:, 32:])
+    assert np.array_equal(normed[2], plain[2])
+    none = oracle_mod.fused_rmsnorm(_bits(x), _bits(wcat), (64, 36, 16), (0, 0, 0), [None] * 3, 1e-6, oracle_mod.BF16)
+    assert all(np.array_equal(p, q) for p, q in zip(none, plain))
+    assert not np.array_equal(normed[0], plain[0])
+
+
+def test_rmsnorm_pins_reject_planted_mistakes(oracle_mod):
+    """The closed form tells the right normalization from plausible wrong ones:
+    the sum instead of the mean, the norm without the square root, eps outside it."""
+    y = np.array([3.0, 4.0])
+    right = y / np.sqrt(np.mean(y ** 2) + 0.5)
+    for wrong in (y / np.sqrt(np.sum(y ** 2) + 0.5), y / (np.mean(y ** 2) + 0.5),
+                  y / (np.sqrt(np.mean(y ** 2)) + 0.5)):
+        assert not np.allclose(wrong, right, rtol=1e-3)
+    assert np.allclose(right, np.array([3.0, 4.0]) / np.sqrt(13.0), rtol=0, atol=1e-15)
