@@ -30,7 +30,8 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 MAX_SPLITS = 8
 MAX_M = 64
 
-EXPORTED = ("proj_fused_gemm", "proj_fused_gemm_prefetch", "proj_separate_gemm", "proj_pack_weights", "proj_pack_check",
+EXPORTED = ("proj_fused_gemm", "proj_fused_gemm_prefetch", "proj_fused_gemm_rmsnorm", "proj_rmsnorm_workspace_bytes",
+            "proj_separate_gemm", "proj_pack_weights", "proj_pack_check",
             "proj_supported", "proj_describe_plan", "proj_set_options", "proj_get_options",
             "proj_check_device_error", "proj_launch_count", "proj_last_error_string", "proj_version")
 
@@ -84,6 +85,12 @@ def lib() -> ctypes.CDLL:
     L.proj_fused_gemm_prefetch.restype = ctypes.c_int
     L.proj_pack_weights.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, ctypes.c_int, vp, vp]
     L.proj_pack_weights.restype = ctypes.c_int
+    L.proj_fused_gemm_rmsnorm.argtypes = [vp, vp, ctypes.POINTER(i32), i32, ctypes.POINTER(i32), ctypes.POINTER(vp),
+                                          ctypes.c_float, ctypes.POINTER(vp), i32, i32, ctypes.c_int, vp,
+                                          ctypes.c_size_t, vp]
+    L.proj_fused_gemm_rmsnorm.restype = ctypes.c_int
+    L.proj_rmsnorm_workspace_bytes.argtypes = [i32, i32, ctypes.POINTER(i32), i32, ctypes.POINTER(i32), ctypes.c_int]
+    L.proj_rmsnorm_workspace_bytes.restype = ctypes.c_size_t
     L.proj_pack_check.argtypes = [vp, vp, i64, i32, i32, i32, ctypes.c_int]
     L.proj_pack_check.restype = ctypes.c_int
     L.proj_supported.argtypes = [i32, i32, i32, ctypes.c_int]
@@ -195,6 +202,46 @@ def fused_gemm_prefetch(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[i
     def fn(xp, wp, sp, op, M, K, dt, st):
         fused_gemm_prefetch_ptr(xp, wp, sp, op, M, K, dt, ranges, st)
     return _gemm(fn, x, w_cat, splits, outs, tf32, stream)
+
+
+def rmsnorm_workspace_bytes(M: int, K: int, splits: Sequence[int], norm_cols: Sequence[int], dtype: int = 0) -> int:
+    """Workspace bytes of proj_fused_gemm_rmsnorm for this shape (raises if unsupported)."""
+    ns = (ctypes.c_int32 * len(splits))(*[int(v) for v in splits])
+    nc = (ctypes.c_int32 * len(norm_cols))(*[int(v) for v in norm_cols])
+    n = int(lib().proj_rmsnorm_workspace_bytes(int(M), int(K), ns, len(splits), nc, int(dtype)))
+    if n == 0:
+        raise ProjError(2, lib().proj_last_error_string().decode())
+    return n
+
+
+def fused_gemm_rmsnorm_ptr(x_ptr: int, w_ptr: int, splits: Sequence[int], norm_cols: Sequence[int],
+                           gamma_ptrs: Sequence[int], eps: float, out_ptrs: Sequence[int], M: int, K: int, dtype: int,
+                           ws_ptr: int, ws_bytes: int, stream_ptr: int = 0) -> None:
+    ns = (ctypes.c_int32 * len(splits))(*[int(v) for v in splits])
+    nc = (ctypes.c_int32 * len(norm_cols))(*[int(v) for v in norm_cols])
+    gp = (ctypes.c_void_p * len(gamma_ptrs))(*[int(p) if p else None for p in gamma_ptrs])
+    po = (ctypes.c_void_p * len(out_ptrs))(*[int(p) for p in out_ptrs])
+    _check(lib().proj_fused_gemm_rmsnorm(x_ptr, w_ptr, ns, len(splits), nc, gp, float(eps), po, M, K, dtype,
+                                         ws_ptr, int(ws_bytes), stream_ptr))
+
+
+def fused_gemm_rmsnorm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int], norm_cols: Sequence[int],
+                       gammas: Sequence[Optional[torch.Tensor]], eps: float, workspace: torch.Tensor,
+                       outs: Optional[List[torch.Tensor]] = None, stream=None):
+    """fused_gemm with the RMSNorm epilogue on the first norm_cols[i] columns of split i.
+    `workspace` is a device byte tensor of at least rmsnorm_workspace_bytes(...) bytes,
+    zeroed once before its first use (each call leaves it ready for the next)."""
+    if len(norm_cols) != len(splits) or len(gammas) != len(splits):
+        raise ProjError(1, "one norm_cols entry and one gamma per split")
+    for g, c in zip(gammas, norm_cols):
+        if c and (g is None or g.dtype != x.dtype or g.numel() < int(c) or not g.is_contiguous()):
+            raise ProjError(1, "gamma of a normalized split must be a dense tensor of the data type")
+    gp = [g.data_ptr() if (g is not None and c) else 0 for g, c in zip(gammas, norm_cols)]
+    ws_bytes = workspace.numel() * workspace.element_size()
+
+    def fn(xp, wp, sp, op, M, K, dt, st):
+        fused_gemm_rmsnorm_ptr(xp, wp, sp, norm_cols, gp, eps, op, M, K, dt, workspace.data_ptr(), ws_bytes, st)
+    return _gemm(fn, x, w_cat, splits, outs, False, stream)
 
 
 def separate_gemm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],

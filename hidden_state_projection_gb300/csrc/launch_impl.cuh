@@ -21,7 +21,12 @@ cudaError_t launch_one(const LaunchReq &r) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!configured[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+        // the opt-in limit covers static and dynamic shared memory together
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
         // clusters of 16 K slices (fp32 rows with many tokens) exceed the portable 8
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);

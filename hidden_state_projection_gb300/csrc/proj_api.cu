@@ -18,6 +18,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -34,7 +35,7 @@ using hsp::LaunchReq;
 using hsp::StreamArgs;
 
 constexpr int kSmemLimit = 232448;          // per-block dynamic shared memory on sm_103
-constexpr int kSmemReserve = 1024 + 512;    // ring alignment slack (1024 for the swizzle) + barriers + flags
+constexpr int kSmemReserve = 1024 + 1024;   // ring alignment slack (1024 for the swizzle) + barriers + flags
 constexpr int kStageWeightBytes = 65536;    // tensor layout: weight bytes per ring stage
 constexpr int kMaxRingStages = 32;
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
@@ -303,7 +304,8 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     p->ring_bytes = p->ring_stages * p->stage_bytes;
     if (p->ring_bytes < red_bytes) p->ring_bytes = red_bytes;
     p->ring_bytes = ceil_div(p->ring_bytes, 128) * 128;
-    p->smem = 1024 + p->ring_bytes + 2 * p->ring_stages * 8 + 8 + 4 * p->ring_stages + 64;
+    // ring, full/empty barriers, abort flag, armed[ring], RMSNorm flags[8], slack
+    p->smem = 1024 + p->ring_bytes + 2 * p->ring_stages * 8 + 8 + 4 * p->ring_stages + 4 * hsp::kMaxSplits + 64;
     proj_plan_info &i = p->info;
     i.bucket = p->bucket;
     i.compute = p->compute;
@@ -529,7 +531,7 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
 // One launch over `n_rows` weight rows starting at `w` (already offset to the first row).
 proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
                         proj_dtype dt, const hsp::SplitTable &splits, const hsp::PrefetchList &pf,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const hsp::NormArgs *norm = nullptr) {
     if (use_umma(M, dt)) return launch_umma_rows(dev, x, w, n_rows, M, K, dt, splits, pf, stream);
     Plan p;
     make_plan(M, K, n_rows, dt, dev.cluster_ctas, &p);
@@ -584,6 +586,7 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
     a.err_word = dev.err_word;
     a.splits = splits;
     a.prefetch = pf;
+    if (norm) a.norm = *norm;
     cudaError_t e = cudaSuccess;
     switch (p.compute) {
         case hsp::kMmaBf16:
@@ -649,9 +652,135 @@ proj_status fused_impl(const void *x, const void *w_cat, const int32_t *n_splits
     return st == PROJ_OK ? ok() : st;
 }
 
+// Co-resident CTAs per cluster size of the current device, for plans made on the
+// host only.  Without a usable device the plan assumes a GB300: 152 SMs, 152 / 152 /
+// 144 / 120 / 112 CTAs co-resident in clusters of 1 / 2 / 4 / 8 / 16.  Leaves the
+// last error string as it was.
+void plan_ctas(int (&ctas)[17]) {
+    static const int kGb300[17] = {0, 152, 152, 0, 144, 0, 0, 0, 120, 0, 0, 0, 0, 0, 0, 0, 112};
+    for (int k = 0; k < 17; ++k) ctas[k] = kGb300[k];
+    char saved[sizeof g_last_error];
+    memcpy(saved, g_last_error, sizeof saved);
+    DeviceInfo d;
+    if (device_info(&d) == PROJ_OK)
+        for (int k = 1; k < 17; ++k) ctas[k] = d.cluster_ctas[k];
+    else
+        (void)cudaGetLastError();
+    memcpy(g_last_error, saved, sizeof saved);
+}
+
+// ---- RMSNorm epilogue: workspace layout ----------------------------------------
+
+// Workspace of one call, in this order: the split counters (one 256-byte block),
+// the parked fp32 values of the normalized columns ([M][cols] per split), the
+// per-CTA sums of squares ([CTAs][M] per split).  A pure function of the shape.
+struct NormLayout {
+    hsp::NormArgs args;     // offsets and CTA ranges (pointers filled in per call)
+    size_t vals_at, part_at, bytes;
+};
+
+proj_status norm_layout(int32_t M, int32_t K, const int32_t *n_splits, int32_t num_splits, const int32_t *norm_cols,
+                        proj_dtype dtype, const int *cluster_ctas, NormLayout *L) {
+    memset(L, 0, sizeof *L);
+    if (!n_splits || !norm_cols) return fail(PROJ_ERR_INVALID_ARG, "n_splits and norm_cols must not be NULL");
+    if (num_splits < 1 || num_splits > PROJ_MAX_SPLITS)
+        return fail(PROJ_ERR_INVALID_ARG, "num_splits=%d (1..%d)", num_splits, PROJ_MAX_SPLITS);
+    if (dtype != PROJ_BF16) return fail(PROJ_ERR_UNSUPPORTED_DTYPE, "the RMSNorm epilogue runs for PROJ_BF16 only");
+    if (M < 1 || M > 8) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "the RMSNorm epilogue runs for 1 <= M <= 8 (M=%d)", M);
+    int64_t n_total = 0;
+    for (int i = 0; i < num_splits; ++i) {
+        if (n_splits[i] < 1) return fail(PROJ_ERR_INVALID_ARG, "n_splits[%d]=%d (need at least 1)", i, n_splits[i]);
+        if (norm_cols[i] < 0 || norm_cols[i] > n_splits[i])
+            return fail(PROJ_ERR_INVALID_ARG, "norm_cols[%d]=%d outside [0, %d]", i, norm_cols[i], n_splits[i]);
+        n_total += n_splits[i];
+    }
+    proj_status st = check_shape(M, K, n_total, dtype);
+    if (st != PROJ_OK) return st;
+    Plan p;
+    make_plan(M, K, static_cast<int>(n_total), dtype, cluster_ctas, &p);
+    if (p.S != 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "the RMSNorm epilogue needs a single-slice plan");
+    hsp::NormArgs &a = L->args;
+    int64_t vals = 0, part = 0;
+    int off = 0;
+    for (int i = 0; i < num_splits; ++i) {
+        a.cols[i] = norm_cols[i];
+        if (norm_cols[i] > 0) {
+            a.active = 1;
+            a.cta_first[i] = off / p.R;
+            a.cta_count[i] = (off + norm_cols[i] - 1) / p.R - a.cta_first[i] + 1;
+            a.vals_off[i] = vals;
+            a.part_off[i] = static_cast<int32_t>(part);
+            vals += static_cast<int64_t>(M) * norm_cols[i];
+            part += static_cast<int64_t>(M) * a.cta_count[i];
+        }
+        off += n_splits[i];
+    }
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    L->vals_at = 256;
+    L->part_at = L->vals_at + up(static_cast<size_t>(vals) * 4);
+    L->bytes = L->part_at + up(static_cast<size_t>(part) * 4);
+    return PROJ_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_splits, int32_t num_splits,
+                                    const int32_t *norm_cols, proj_dtype dtype) {
+    int ctas[17];
+    plan_ctas(ctas);
+    NormLayout L;
+    if (norm_layout(M, K, n_splits, num_splits, norm_cols, dtype, ctas, &L) != PROJ_OK) return 0;
+    return L.bytes;
+}
+
+proj_status proj_fused_gemm_rmsnorm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                                    const int32_t *norm_cols, const void *const *gammas, float eps,
+                                    void *const *outs, int32_t M, int32_t K, proj_dtype dtype, void *workspace,
+                                    size_t workspace_bytes, proj_stream_t stream) {
+    int64_t n_total = 0;
+    proj_status st = validate(x, w_cat, n_splits, num_splits, outs, M, K, dtype, &n_total);
+    if (st != PROJ_OK) return st;
+    if (M == 0) return ok();
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(PROJ_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (!gammas) return fail(PROJ_ERR_INVALID_ARG, "gammas must not be NULL");
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != PROJ_OK) return st;
+    NormLayout L;
+    if ((st = norm_layout(M, K, n_splits, num_splits, norm_cols, dtype, dev.cluster_ctas, &L)) != PROJ_OK) return st;
+    if (!workspace) return fail(PROJ_ERR_INVALID_ARG, "workspace must not be NULL");
+    if (!aligned16(workspace)) return fail(PROJ_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    if (workspace_bytes < L.bytes)
+        return fail(PROJ_ERR_INVALID_ARG, "workspace of %zu bytes, this call needs %zu", workspace_bytes, L.bytes);
+    hsp::NormArgs a = L.args;
+    for (int i = 0; i < num_splits; ++i) {
+        if (a.cols[i] == 0) continue;
+        if (!gammas[i]) return fail(PROJ_ERR_INVALID_ARG, "gammas[%d] is NULL", i);
+        if (reinterpret_cast<uintptr_t>(gammas[i]) & 1u) return fail(PROJ_ERR_MISALIGNED, "gammas[%d] is not 2-byte aligned", i);
+        a.gamma[i] = gammas[i];
+    }
+    a.eps = eps;
+    char *ws = static_cast<char *>(workspace);
+    a.counter = reinterpret_cast<unsigned *>(ws);
+    a.vals = reinterpret_cast<float *>(ws + L.vals_at);
+    a.partial = reinterpret_cast<float *>(ws + L.part_at);
+    hsp::SplitTable t;
+    memset(&t, 0, sizeof t);
+    t.count = num_splits;
+    int off = 0;
+    for (int i = 0; i < num_splits; ++i) {
+        t.off[i] = off;
+        t.rows[i] = n_splits[i];
+        t.out[i] = outs[i];
+        off += n_splits[i];
+    }
+    hsp::PrefetchList none;
+    memset(&none, 0, sizeof none);
+    st = launch_rows(dev, x, w_cat, static_cast<int>(n_total), M, K, dtype, t, none,
+                     reinterpret_cast<cudaStream_t>(stream), a.active ? &a : nullptr);
+    return st == PROJ_OK ? ok() : st;
+}
 
 proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
                             void *const *outs, int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream) {
@@ -746,19 +875,8 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
     proj_status st = check_shape(M, K, n_rows, dtype);
     if (st != PROJ_OK) return st;
     if (M < 1 || n_rows < 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "M and n_rows must be at least 1");
-    // Without a usable device the plan assumes a GB300: 152 SMs, 152 / 152 / 144 /
-    // 120 / 112 CTAs co-resident in clusters of 1 / 2 / 4 / 8 / 16.
-    int ctas[17] = {0, 152, 152, 0, 144, 0, 0, 0, 120, 0, 0, 0, 0, 0, 0, 0, 112};
-    {
-        char saved[sizeof g_last_error];
-        memcpy(saved, g_last_error, sizeof saved);
-        DeviceInfo d;
-        if (device_info(&d) == PROJ_OK)
-            for (int k = 1; k < 17; ++k) ctas[k] = d.cluster_ctas[k];
-        else
-            (void)cudaGetLastError();
-        memcpy(g_last_error, saved, sizeof saved);
-    }
+    int ctas[17];
+    plan_ctas(ctas);
     if (use_umma(M, dtype)) {
         UPlan u;
         make_umma_plan(M, K, n_rows, dtype, &u);

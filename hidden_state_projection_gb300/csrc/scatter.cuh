@@ -19,11 +19,17 @@ struct OutRow {
     int64_t stride_bytes;
 };
 
-template <bool BF16_OUT>
-__device__ __forceinline__ OutRow out_row(const SplitTable &s, int n) {
+// The split that row n of the launch belongs to.
+__device__ __forceinline__ int split_of(const SplitTable &s, int n) {
     int i = 0;
 #pragma unroll 1
     while (i + 1 < s.count && n >= s.off[i + 1]) ++i;
+    return i;
+}
+
+template <bool BF16_OUT>
+__device__ __forceinline__ OutRow out_row(const SplitTable &s, int n) {
+    const int i = split_of(s, n);
     constexpr int esz = BF16_OUT ? 2 : 4;
     OutRow o;
     o.base = static_cast<char *>(s.out[i]) + static_cast<int64_t>(n - s.off[i]) * esz;

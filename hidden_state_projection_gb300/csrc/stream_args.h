@@ -31,6 +31,27 @@ struct SplitTable {
     void *out[kMaxSplits];
 };
 
+// RMSNorm epilogue (q_norm / kv_norm of the projections' consumers): split i's
+// first cols[i] columns are normalized per token, y * rsqrt(mean(y^2) + eps) * gamma,
+// from the fp32 sums, and rounded once.  The mean spans CTAs, so the CTAs meeting a
+// normalized split park their fp32 values and per-token sums of squares in a
+// workspace; the last of them to arrive (an arrival counter per split) adds the sums
+// in CTA order, normalizes every value of the split and stores it, then clears the
+// counter.  Single-slice (S = 1) launches only.
+struct NormArgs {
+    int32_t active;                 // 1: some split is normalized
+    float eps;
+    int32_t cols[kMaxSplits];       // normalized leading columns of split i (0: none)
+    const void *gamma[kMaxSplits];  // [cols[i]] elements of the data type
+    int64_t vals_off[kMaxSplits];   // float offset of split i's [M][cols[i]] block in vals
+    int32_t part_off[kMaxSplits];   // float offset of split i's [cta_count[i]][M] block in partial
+    int32_t cta_first[kMaxSplits];  // first CTA (grid.x index) holding a normalized row of split i
+    int32_t cta_count[kMaxSplits];  // CTAs holding normalized rows of split i
+    float *vals;                    // workspace
+    float *partial;                 // workspace
+    unsigned *counter;              // workspace, [kMaxSplits], zero between calls
+};
+
 // K is cut into units of 128 bytes.  Unit u is summed by warp (u mod WK) of the
 // CTA that owns its K slice (slice s holds units [s*units_per_slice, ...)); a
 // ring stage carries stage_units consecutive units of every row of the CTA and
@@ -67,6 +88,7 @@ struct StreamArgs {
     int *err_word;             // device error word (PROJ_ERR_TIMEOUT on expiry)
     SplitTable splits;
     PrefetchList prefetch;
+    NormArgs norm;
 };
 
 // Tensor-memory path (9 <= M <= 64): a CTA owns a 128-row weight tile and one

@@ -281,6 +281,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             atomicCAS(a.err_word, 0, kDeviceErrTimeout);
             *abort_flag = 1;
         }
+        // First half of the closing cluster barrier: my receive buffer is complete, so
+        // every copy out of a peer's staging buffer into mine has landed.  The wait
+        // comes last, after the trigger: no CTA leaves while a bulk copy may still read
+        // its staging buffer, yet the peers' sums, stores and fences overlap it.
+        cluster_arrive();
         if (!aborted && got) {
             constexpr int kT4 = NT / 4;
             // consecutive threads take consecutive rows of the same four tokens
@@ -319,9 +324,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem_d, C::kTmemCols);
     }
-    // No CTA leaves while a peer's bulk copy may still read its staging buffer: every
-    // CTA arrives here only after its own receive barrier completed.
-    if (a.slices > 1) cluster_sync_all();
+    if (a.slices > 1) cluster_wait();
 }
 
 }  // namespace hsp

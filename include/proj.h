@@ -35,6 +35,7 @@
 #ifndef HSP_PROJ_H
 #define HSP_PROJ_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -168,6 +169,40 @@ proj_status proj_fused_gemm_prefetch(const void *x, const void *w_cat, const int
                                      int32_t num_splits, void *const *outs, int32_t M, int32_t K,
                                      proj_dtype dtype, const proj_prefetch_range *ranges,
                                      int32_t num_ranges, proj_stream_t stream);
+
+/*
+ * proj_fused_gemm_rmsnorm -- proj_fused_gemm followed, in the same kernel, by the
+ * RMSNorm its consumers apply (TensorRT-LLM PR #20636, Description: the q_norm /
+ * kv_norm RMSNorms read the wq_a / wkv outputs; PR #20502, glm_mla_kv_half_append
+ * commit message: RMSNorm of the 512 latent columns of the raw kv_a_proj output).
+ * For split i with c = norm_cols[i] > 0, every token m and r < c:
+ *     outs[i][m, r] = round(y[m, r] / sqrt(mean_{j < c} y[m, j]^2 + eps) * gammas[i][r])
+ * with y the fp32 sums of the projection (one rounding per output); columns r >= c,
+ * and splits with norm_cols[i] == 0, are the plain projection, bitwise those of
+ * proj_fused_gemm.
+ *   norm_cols  host [num_splits], each in [0, n_splits[i]]
+ *   gammas     host array of num_splits device pointers; gammas[i] is [norm_cols[i]]
+ *              of the data type (may be NULL where norm_cols[i] == 0)
+ *   eps        finite, >= 0
+ *   workspace  device, 16-byte aligned, at least proj_rmsnorm_workspace_bytes(...)
+ *              bytes, owned by the caller.  Zero it once before its first use; every
+ *              call leaves it ready for the next (its counters back at zero).  Calls
+ *              that share a workspace must not overlap on the GPU.  After a call that
+ *              reported PROJ_ERR_TIMEOUT, zero it again.
+ * PROJ_BF16 with 1 <= M <= 8 only (PROJ_ERR_UNSUPPORTED_DTYPE / _SHAPE otherwise).
+ * Bitwise identical run to run and under CUDA-graph replay.
+ */
+proj_status proj_fused_gemm_rmsnorm(const void *x, const void *w_cat, const int32_t *n_splits,
+                                    int32_t num_splits, const int32_t *norm_cols,
+                                    const void *const *gammas, float eps, void *const *outs,
+                                    int32_t M, int32_t K, proj_dtype dtype, void *workspace,
+                                    size_t workspace_bytes, proj_stream_t stream);
+
+/* Workspace bytes proj_fused_gemm_rmsnorm needs for this shape (host only; 0 when the
+ * shape is not supported, with proj_last_error_string saying why). */
+size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_splits,
+                                    int32_t num_splits, const int32_t *norm_cols,
+                                    proj_dtype dtype);
 
 /*
  * proj_separate_gemm -- one launch per projection over its row range of the same

@@ -166,3 +166,16 @@ def test_prefetch_entry_validation(hsp):
     assert call([(0x40008, 64)], 1) == S["PROJ_ERR_MISALIGNED"]
     assert call([(0x40000, 60)], 1) == S["PROJ_ERR_MISALIGNED"]
     assert call([(0x40000, 0)], 1) == S["PROJ_ERR_INVALID_ARG"]
+
+
+def test_rmsnorm_workspace_size(hsp):
+    """Workspace sizing is host-only: counters, parked fp32 values [M][cols] per split
+    and per-CTA sums; 0 (with a reason) for shapes the epilogue does not run."""
+    n = hsp.rmsnorm_workspace_bytes(1, 5120, (1280, 512), (1280, 512))
+    assert n >= 256 + (1280 + 512) * 4 and n % 256 == 0
+    assert hsp.rmsnorm_workspace_bytes(8, 5120, (1280, 512), (1280, 512)) >= 256 + 8 * (1280 + 512) * 4
+    assert hsp.rmsnorm_workspace_bytes(1, 5120, (1280, 512), (0, 0)) == 256
+    for bad in ((9, 5120, (1280, 512), (1280, 512), 0), (1, 5120, (1280, 512), (1281, 512), 0),
+                (1, 5120, (1280, 512), (1280, 512), 1)):
+        with pytest.raises(hsp.ProjError):
+            hsp.rmsnorm_workspace_bytes(*bad)
