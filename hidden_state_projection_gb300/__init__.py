@@ -31,6 +31,7 @@ MAX_SPLITS = 8
 MAX_M = 64
 
 EXPORTED = ("proj_fused_gemm", "proj_fused_gemm_prefetch", "proj_fused_gemm_rmsnorm", "proj_rmsnorm_workspace_bytes",
+            "proj_fused_gemm_rmsnorm_static",
             "proj_separate_gemm", "proj_pack_weights", "proj_pack_check",
             "proj_supported", "proj_describe_plan", "proj_set_options", "proj_get_options",
             "proj_check_device_error", "proj_launch_count", "proj_last_error_string", "proj_version")
@@ -89,6 +90,10 @@ def lib() -> ctypes.CDLL:
                                           ctypes.c_float, ctypes.POINTER(vp), i32, i32, ctypes.c_int, vp,
                                           ctypes.c_size_t, vp]
     L.proj_fused_gemm_rmsnorm.restype = ctypes.c_int
+    L.proj_fused_gemm_rmsnorm_static.argtypes = [vp, vp, ctypes.POINTER(i32), i32, ctypes.POINTER(i32),
+                                                 ctypes.POINTER(vp), ctypes.c_float, ctypes.POINTER(vp), i32, i32,
+                                                 ctypes.c_int, vp]
+    L.proj_fused_gemm_rmsnorm_static.restype = ctypes.c_int
     L.proj_rmsnorm_workspace_bytes.argtypes = [i32, i32, ctypes.POINTER(i32), i32, ctypes.POINTER(i32), ctypes.c_int]
     L.proj_rmsnorm_workspace_bytes.restype = ctypes.c_size_t
     L.proj_pack_check.argtypes = [vp, vp, i64, i32, i32, i32, ctypes.c_int]

@@ -55,6 +55,14 @@ std::atomic<int> g_opt_small_m_path{0};
 // Device error word: a kernel whose bounded wait runs out stores PROJ_ERR_TIMEOUT here.
 __device__ int g_hsp_device_error;
 
+namespace hsp {
+// Sets the text proj_last_error_string returns (for entry points in other files).
+proj_status set_last_error(proj_status st, const char *msg) {
+    snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+    return st;
+}
+}  // namespace hsp
+
 namespace {
 
 proj_status fail(proj_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));

@@ -205,6 +205,32 @@ size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_split
                                     proj_dtype dtype);
 
 /*
+ * proj_fused_gemm_rmsnorm_static -- proj_fused_gemm_rmsnorm for callers that cannot
+ * allocate device memory.  The pages have no counterpart; it exists for callers
+ * that have no workspace to pass: code under an inference runtime that owns all
+ * device memory through its own pool and forbids side allocations, plugins that
+ * receive only the tensors of one operation, and latency-critical paths where
+ * cudaMalloc's implicit device synchronisation is not acceptable.  It allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library call): the workspace is
+ * a fixed 1 MiB array compiled into this library, present in the memory of every GPU
+ * that loads it until the process exits.  The caller still passes inputs and outputs,
+ * with the meaning and limits of proj_fused_gemm_rmsnorm.
+ *   - The first call made with a given device current looks up the array's device
+ *     address on that device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array and finds the last call's contents in it; each
+ *     call clears the part that must start at zero (cudaMemsetAsync on `stream`)
+ *     before its kernel.  Calls that overlap on the GPU race on the array: issue
+ *     them on one stream, or order them.
+ *   - Shapes whose workspace (proj_rmsnorm_workspace_bytes) exceeds 1 MiB are refused
+ *     with PROJ_ERR_UNSUPPORTED_SHAPE and a message that gives both sizes.
+ */
+proj_status proj_fused_gemm_rmsnorm_static(const void *x, const void *w_cat, const int32_t *n_splits,
+                                           int32_t num_splits, const int32_t *norm_cols,
+                                           const void *const *gammas, float eps, void *const *outs,
+                                           int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream);
+
+/*
  * proj_separate_gemm -- one launch per projection over its row range of the same
  * w_cat (TensorRT-LLM PR #20636, Description: "2-8 tokens: one tinygemm2 per
  * projection").  Same arguments and outputs as proj_fused_gemm, bitwise equal to it.
