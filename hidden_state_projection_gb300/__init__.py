@@ -48,7 +48,7 @@ class Options(ctypes.Structure):
     _fields_ = [("pdl", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
                 ("skip_stage_plus1", ctypes.c_int32), ("large_m_path", ctypes.c_int32),
                 ("l2_prefetch", ctypes.c_int32), ("trigger_early", ctypes.c_int32),
-                ("small_m_path", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
+                ("small_m_path", ctypes.c_int32), ("reg_path", ctypes.c_int32)]
 
 
 class PrefetchRange(ctypes.Structure):
@@ -291,7 +291,7 @@ def describe_plan(M: int, K: int, n_rows: int, dtype: int) -> dict:
 
 def set_options(pdl: Optional[bool] = None, wait_limit_us: int = 0, skip_stage: Optional[int] = None,
                 large_m_path: int = 0, l2_prefetch: bool = False, trigger_early: bool = False,
-                small_m_path: int = 0):
+                small_m_path: int = 0, reg_path: int = 0):
     o = Options()
     o.pdl = -1 if pdl is None else int(bool(pdl))
     o.wait_limit_us = int(wait_limit_us)
@@ -300,6 +300,7 @@ def set_options(pdl: Optional[bool] = None, wait_limit_us: int = 0, skip_stage: 
     o.l2_prefetch = 1 if l2_prefetch else 0
     o.trigger_early = 1 if trigger_early else 0
     o.small_m_path = int(small_m_path)
+    o.reg_path = int(reg_path)
     _check(lib().proj_set_options(ctypes.byref(o)))
 
 
@@ -308,7 +309,7 @@ def get_options() -> dict:
     _check(lib().proj_get_options(ctypes.byref(o)))
     return {"pdl": o.pdl, "wait_limit_us": o.wait_limit_us, "skip_stage_plus1": o.skip_stage_plus1,
             "large_m_path": o.large_m_path, "l2_prefetch": o.l2_prefetch, "trigger_early": o.trigger_early,
-            "small_m_path": o.small_m_path}
+            "small_m_path": o.small_m_path, "reg_path": o.reg_path}
 
 
 def check_device_error(stream=None) -> None:

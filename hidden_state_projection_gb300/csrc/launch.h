@@ -42,6 +42,19 @@ struct UmmaLaunchReq {
 };
 cudaError_t launch_umma(const UmmaLaunchReq &r);
 
+// Register-ring kernel launch (bf16, M <= 8, rows of at most kRegMaxUnits k-units).
+struct RegLaunchReq {
+    dim3 grid;       // (row CTAs, 1, 1)
+    int smem_bytes;  // the token box + 1024 bytes of alignment slack
+    int pdl;
+    cudaStream_t stream;
+    CUtensorMap tmap_x;  // tokens viewed as [units][M][128 bytes], one box for all of them
+    StreamArgs args;     // w, x, row_bytes, n_rows, rows_per_cta, M, units_total, hooks, splits, prefetch, norm
+};
+cudaError_t launch_reg(const RegLaunchReq &r);
+constexpr int kRegThreadsHost = 16 * 32;
+constexpr int kRegDepthHost = 5;
+
 // Threads per CTA of a bucket (eight consumer warps + one producer warp).
 constexpr int kThreadsPerCta = 9 * 32;
 constexpr int kUmmaThreadsHost = 128;

@@ -11,9 +11,9 @@ namespace hsp {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxDynamicSmem = 232448;  // 227 KiB, the per-block opt-in limit of sm_103
 
-template <int COMPUTE, int MT, int RT, int WR, int WK, bool TENSOR>
+template <int COMPUTE, int MT, int RT, int WR, int WK, bool TENSOR, bool NORM>
 cudaError_t launch_one(const LaunchReq &r) {
-    auto kern = hsp_stream_kernel<COMPUTE, MT, RT, WR, WK, TENSOR>;
+    auto kern = hsp_stream_kernel<COMPUTE, MT, RT, WR, WK, TENSOR, NORM>;
     // The shared-memory opt-in is per function and per device; set it once.
     static std::atomic<unsigned char> configured[kMaxDevices];
     int dev = 0;
@@ -59,7 +59,16 @@ cudaError_t launch_one(const LaunchReq &r) {
 
 template <int COMPUTE, int MT, int RT, int WR, int WK>
 cudaError_t launch_variant(const LaunchReq &r) {
-    return r.tensor ? launch_one<COMPUTE, MT, RT, WR, WK, true>(r) : launch_one<COMPUTE, MT, RT, WR, WK, false>(r);
+    if constexpr (COMPUTE == kMmaBf16 && MT == 1) {
+        // the RMSNorm epilogue (bf16, M <= 8) has instances of its own
+        if (r.args.norm.active)
+            return r.tensor ? launch_one<COMPUTE, MT, RT, WR, WK, true, true>(r)
+                            : launch_one<COMPUTE, MT, RT, WR, WK, false, true>(r);
+    } else {
+        if (r.args.norm.active) return cudaErrorInvalidConfiguration;
+    }
+    return r.tensor ? launch_one<COMPUTE, MT, RT, WR, WK, true, false>(r)
+                    : launch_one<COMPUTE, MT, RT, WR, WK, false, false>(r);
 }
 
 template <int COMPUTE>

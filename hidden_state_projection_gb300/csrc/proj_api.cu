@@ -8,6 +8,9 @@
 //   bucket 0, M <= 8      : 1 token tile;  warps split K 8 ways, no K slices
 //   bucket 1, 9 <= M <= 32: 2 or 4 token tiles; 2 row warps x 4 K warps, S K slices
 //   bucket 2, 33 <= M <= 64: 8 token tiles; 4 row warps x 2 K warps, S K slices
+// bf16 with M <= 8 and rows of at most 80 k-units of 128 bytes (K <= 5120) runs the
+// register-ring kernel instead (sixteen warps split K, weights straight into
+// registers), measured faster on GB300 there.
 // The K-split (warps WK, slices S, box width) is a function of (K, dtype,
 // bucket) only, so an output row is summed in the same order whatever the
 // number of rows in the launch -- the property that makes the fused and the
@@ -49,6 +52,7 @@ std::atomic<int> g_opt_large_m_path{0};
 std::atomic<int> g_opt_l2_prefetch{0};
 std::atomic<int> g_opt_trigger_early{0};
 std::atomic<int> g_opt_small_m_path{0};
+std::atomic<int> g_opt_reg_path{0};
 
 }  // namespace
 
@@ -536,11 +540,110 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
     return PROJ_OK;
 }
 
+// ---- register-ring plan (bf16, M <= 8) -------------------------------------
+
+// The register-ring kernel serves bf16 with M <= 8 when a row is a whole number of
+// 128-byte k-units and, by default, at most kRegAutoUnits of them: then the sixteen
+// warps hold a CTA's whole share of the weights in flight at once (measured on GB300,
+// wq_a++wkv K = 5120: 5.41 / 5.62 / 5.76 us at M = 1 / 4 / 8 against 6.10 / 6.10 /
+// 6.18 us for the streaming kernel; at K = 7168 it is no faster).  Option reg_path 1
+// turns it off, 2 uses it up to kRegMaxUnits.  The choice depends on (M, K, dtype)
+// only, so fused and per-projection launches run the same kernel.
+constexpr int kRegAutoUnits = 80;
+constexpr int kRegMaxUnits = 128;
+
+bool use_reg(int M, int K, proj_dtype dt) {
+    if (dt != PROJ_BF16 || M < 1 || M > 8) return false;
+    const int64_t row_bytes = static_cast<int64_t>(K) * 2;
+    if (row_bytes % hsp::kUnitBytes != 0) return false;
+    const int o = g_opt_reg_path.load();
+    if (o == 1) return false;
+    if (M <= 2 && g_opt_small_m_path.load() == 1) return false;  // the opt-in CUDA-core path
+    return row_bytes / hsp::kUnitBytes <= (o == 2 ? kRegMaxUnits : kRegAutoUnits);
+}
+
+struct RegPlan {
+    int R, grid, units, smem;
+};
+
+void make_reg_plan(int M, int K, int n_rows, int sms, RegPlan *p) {
+    p->units = static_cast<int>(static_cast<int64_t>(K) * 2 / hsp::kUnitBytes);
+    p->R = std::min(16, std::max(1, ceil_div(n_rows, std::max(1, sms))));
+    p->grid = ceil_div(n_rows, p->R);
+    p->smem = p->units * M * hsp::kUnitBytes + 1024;
+}
+
+void reg_plan_info(int M, int K, const RegPlan &p, proj_plan_info *i) {
+    memset(i, 0, sizeof *i);
+    i->bucket = 0;
+    i->compute = hsp::kMmaBf16;
+    i->rows_per_cta = p.R;
+    i->row_ctas = p.grid;
+    i->slices = 1;
+    i->k_warps = 16;
+    i->row_warps = 1;
+    i->row_tiles = 1;
+    i->token_tiles = 1;
+    i->ring_stages = hsp::kRegDepthHost;  // k-units in flight per warp
+    i->stage_bytes = 0;
+    i->smem_bytes = p.smem;
+    i->k_per_stage = hsp::kUnitBytes / 2;
+    i->stages_total = ceil_div(p.units, 16);  // k-units per warp
+    i->threads = hsp::kRegThreadsHost;
+    i->units_per_slice = p.units;
+    i->engine = 2;
+    i->tensor_copies = 1;  // the tokens arrive as one tensor copy
+    (void)M;
+    (void)K;
+}
+
+proj_status launch_reg_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
+                            const hsp::SplitTable &splits, const hsp::PrefetchList &pf, cudaStream_t stream,
+                            const hsp::NormArgs *norm) {
+    RegPlan p;
+    make_reg_plan(M, K, n_rows, dev.sms, &p);
+    hsp::RegLaunchReq r{};
+    // tokens as [units][M][128 bytes] (row stride row_bytes, unit stride 128 bytes), one box
+    const uint64_t row_bytes = static_cast<uint64_t>(K) * 2;
+    const uint64_t xdims[3] = {64u, static_cast<uint64_t>(M), static_cast<uint64_t>(p.units)};
+    const uint64_t strides[2] = {row_bytes, 128u};
+    const uint32_t xbox[3] = {64u, static_cast<uint32_t>(M), static_cast<uint32_t>(p.units)};
+    proj_status st = encode_map(x, 3, xdims, strides, xbox, PROJ_BF16, &r.tmap_x);
+    if (st != PROJ_OK) return st;
+    r.grid = dim3(static_cast<unsigned>(p.grid), 1, 1);
+    r.smem_bytes = p.smem;
+    r.pdl = g_opt_pdl.load();
+    r.stream = stream;
+    StreamArgs &a = r.args;
+    a.w = static_cast<const char *>(w);
+    a.x = static_cast<const char *>(x);
+    a.row_bytes = static_cast<int64_t>(row_bytes);
+    a.n_rows = n_rows;
+    a.rows_per_cta = p.R;
+    a.M = M;
+    a.units_total = p.units;
+    a.units_per_slice = p.units;
+    a.slices = 1;
+    a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
+    a.trigger_early = g_opt_trigger_early.load();
+    const int wus = g_opt_wait_us.load();
+    a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
+    a.err_word = dev.err_word;
+    a.splits = splits;
+    a.prefetch = pf;
+    if (norm) a.norm = *norm;
+    cudaError_t e = hsp::launch_reg(r);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch (register-ring path)");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PROJ_OK;
+}
+
 // One launch over `n_rows` weight rows starting at `w` (already offset to the first row).
 proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
                         proj_dtype dt, const hsp::SplitTable &splits, const hsp::PrefetchList &pf,
                         cudaStream_t stream, const hsp::NormArgs *norm = nullptr) {
     if (use_umma(M, dt)) return launch_umma_rows(dev, x, w, n_rows, M, K, dt, splits, pf, stream);
+    if (use_reg(M, K, dt)) return launch_reg_rows(dev, x, w, n_rows, M, K, splits, pf, stream, norm);
     Plan p;
     make_plan(M, K, n_rows, dt, dev.cluster_ctas, &p);
     if (p.ring_stages < 1 || p.smem > kSmemLimit)
@@ -704,9 +807,18 @@ proj_status norm_layout(int32_t M, int32_t K, const int32_t *n_splits, int32_t n
     }
     proj_status st = check_shape(M, K, n_total, dtype);
     if (st != PROJ_OK) return st;
-    Plan p;
-    make_plan(M, K, static_cast<int>(n_total), dtype, cluster_ctas, &p);
-    if (p.S != 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "the RMSNorm epilogue needs a single-slice plan");
+    // rows per CTA of the kernel that will run (the CTA ranges below depend on it)
+    int R = 0;
+    if (use_reg(M, K, dtype)) {
+        RegPlan rp;
+        make_reg_plan(M, K, static_cast<int>(n_total), cluster_ctas[1], &rp);
+        R = rp.R;
+    } else {
+        Plan p;
+        make_plan(M, K, static_cast<int>(n_total), dtype, cluster_ctas, &p);
+        if (p.S != 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "the RMSNorm epilogue needs a single-slice plan");
+        R = p.R;
+    }
     hsp::NormArgs &a = L->args;
     int64_t vals = 0, part = 0;
     int off = 0;
@@ -714,8 +826,8 @@ proj_status norm_layout(int32_t M, int32_t K, const int32_t *n_splits, int32_t n
         a.cols[i] = norm_cols[i];
         if (norm_cols[i] > 0) {
             a.active = 1;
-            a.cta_first[i] = off / p.R;
-            a.cta_count[i] = (off + norm_cols[i] - 1) / p.R - a.cta_first[i] + 1;
+            a.cta_first[i] = off / R;
+            a.cta_count[i] = (off + norm_cols[i] - 1) / R - a.cta_first[i] + 1;
             a.vals_off[i] = vals;
             a.part_off[i] = static_cast<int32_t>(part);
             vals += static_cast<int64_t>(M) * norm_cols[i];
@@ -891,6 +1003,12 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
         *info = u.info;
         return ok();
     }
+    if (use_reg(M, K, dtype)) {
+        RegPlan rp;
+        make_reg_plan(M, K, n_rows, ctas[1], &rp);
+        reg_plan_info(M, K, rp, info);
+        return ok();
+    }
     Plan p;
     make_plan(M, K, n_rows, dtype, ctas, &p);
     *info = p.info;
@@ -903,9 +1021,10 @@ proj_status proj_set_options(const proj_options *opt) {
     if (opt->wait_limit_us < 0 || opt->skip_stage_plus1 < 0)
         return fail(PROJ_ERR_INVALID_ARG, "wait_limit_us and skip_stage_plus1 must be >= 0");
     if (opt->large_m_path < 0 || opt->large_m_path > 2 || opt->l2_prefetch < 0 || opt->l2_prefetch > 1 ||
-        opt->trigger_early < 0 || opt->trigger_early > 1 || opt->small_m_path < 0 || opt->small_m_path > 1)
+        opt->trigger_early < 0 || opt->trigger_early > 1 || opt->small_m_path < 0 || opt->small_m_path > 1 ||
+        opt->reg_path < 0 || opt->reg_path > 2)
         return fail(PROJ_ERR_INVALID_ARG,
-                    "large_m_path must be 0, 1 or 2; small_m_path, l2_prefetch and trigger_early 0 or 1");
+                    "large_m_path and reg_path must be 0, 1 or 2; small_m_path, l2_prefetch and trigger_early 0 or 1");
     if (opt->pdl >= 0) g_opt_pdl.store(opt->pdl);
     g_opt_wait_us.store(opt->wait_limit_us);
     g_opt_skip_stage_plus1.store(opt->skip_stage_plus1);
@@ -913,6 +1032,7 @@ proj_status proj_set_options(const proj_options *opt) {
     g_opt_l2_prefetch.store(opt->l2_prefetch);
     g_opt_trigger_early.store(opt->trigger_early);
     g_opt_small_m_path.store(opt->small_m_path);
+    g_opt_reg_path.store(opt->reg_path);
     return ok();
 }
 
@@ -926,6 +1046,7 @@ proj_status proj_get_options(proj_options *opt) {
     opt->l2_prefetch = g_opt_l2_prefetch.load();
     opt->trigger_early = g_opt_trigger_early.load();
     opt->small_m_path = g_opt_small_m_path.load();
+    opt->reg_path = g_opt_reg_path.load();
     return ok();
 }
 

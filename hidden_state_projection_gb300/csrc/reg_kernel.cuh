@@ -1,0 +1,209 @@
+// reg_kernel.cuh -- the register-ring projection kernel (bf16, 1 <= M <= 8, short rows).
+//
+// Same operation and split epilogue as the streaming kernel (TensorRT-LLM PR #20636,
+// Description: one GEMM over the row-concatenated weight, its halves returned as
+// dense [M, N_i] outputs), laid out for the case where a CTA's whole share of the
+// weights can be in flight at once in registers: rows of at most 80 k-units of
+// 128 bytes (K <= 5120 bf16, the wq_a / wkv hidden size) and at most 16 rows per CTA.
+//
+//   * sixteen warps; warp w owns the k-units u = w, w + 16, ... of every row of the
+//     CTA.  Lane (g, q) = (lane / 4, lane % 4) loads, per unit, the 16-byte pieces
+//     [32h + 8q, 32h + 8q + 8) (h = 0, 1) of rows g and g + 8 straight into registers
+//     (read-only path, no L1 allocation, L2 evict-first), kRegDepth units ahead.  The
+//     first kRegDepth units are requested before griddepcontrol.wait, at kernel entry:
+//     no copy descriptor, barrier or shared-memory stage sits between the launch and
+//     the first weight request;
+//   * the tokens X[M, K] arrive after the grid-dependency wait as ONE 3-D tensor copy
+//     [units][M][128 bytes] with the 128-byte swizzle into shared memory (the tensor
+//     copy bypasses L1, which keeps the whole L1 for the weight requests in flight);
+//   * the eight bf16 of a 16-byte piece feed two mma.sync m16n8k16: the k positions
+//     of the A fragment (weights, 16 rows) and of the B fragment (tokens, 8 columns)
+//     are the same permutation of the unit's k, so each product is the dot product
+//     over the unit.  Two accumulator chains (the x/y and the z/w halves of every
+//     piece) are added at the end;
+//   * the 16 warp partials of every output are added in warp order, rounded once to
+//     bf16 and scattered into the split outputs (or parked for the RMSNorm epilogue);
+//     every storing thread fences, the CTA synchronises, and only then is the
+//     dependent launch triggered (the trigger follows the stores).
+//
+// Determinism: an output's sum depends only on K (the unit -> warp map and the chain
+// split), never on the row count, the row's slot or the grid, so fused and
+// per-projection launches, repeats and graph replays give identical bits.
+//
+// Rows past the CTA's rows and tokens past M are never loaded (zero registers /
+// repeated token rows); their products are never stored.  The one barrier wait (the
+// token copy) is bounded; on expiry the kernel records PROJ_ERR_TIMEOUT, skips its
+// stores, waits (bounded) for its copy if it was issued, and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "norm_epilogue.cuh"
+#include "prefetch.cuh"
+#include "ptx.cuh"
+#include "scatter.cuh"
+#include "stream_args.h"
+
+namespace hsp {
+
+constexpr int kRegWarps = 16;
+constexpr int kRegThreads = kRegWarps * 32;
+constexpr int kRegDepth = 5;     // k-units of weights in flight per warp
+constexpr int kRegMaxRows = 16;  // rows per CTA (one 16-row MMA tile)
+
+// 16 bytes of weights through the read-only path, not allocated in L1, with an L2
+// evict-first policy and 256-byte L2 fetches.
+__device__ __forceinline__ uint4 ldg_weights(const char *p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
+// Warp-wide bounded wait on one barrier phase (true when it completed in time).
+__device__ __forceinline__ bool reg_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        const bool ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        int give_up = 0;
+        if ((it & 7u) == 7u) give_up = (global_timer_ns() - t0 > limit_ns) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+}
+
+// NORM: the RMSNorm epilogue is compiled in (the instance without it carries no
+// call, parked-value branch or flag of it).
+template <int D, bool NORM>
+__global__ void __launch_bounds__(kRegThreads, 1)
+    hsp_reg_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ StreamArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];    // the token box (1024-aligned inside)
+    __shared__ float part[kRegWarps][kRegMaxRows][8];         // warp partials [warp][row slot][token]
+    __shared__ float sums[kRegMaxRows * 8];                   // CTA sums [row slot][token] (RMSNorm)
+    __shared__ int finish[kMaxSplits];
+    __shared__ __align__(8) uint64_t xfull;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int row0 = blockIdx.x * a.rows_per_cta;
+    const int rows_here = min(a.rows_per_cta, a.n_rows - row0);
+    const bool lo_ok = g < rows_here, hi_ok = g + 8 < rows_here;
+    const char *wlo = a.w + static_cast<int64_t>(row0 + (lo_ok ? g : 0)) * a.row_bytes + q * 16;
+    const char *whi = a.w + static_cast<int64_t>(row0 + (hi_ok ? g + 8 : 0)) * a.row_bytes + q * 16;
+    const int nu = a.units_total > warp ? (a.units_total - warp + kRegWarps - 1) / kRegWarps : 0;
+    const uint64_t policy = l2_policy_evict_first();
+
+    // wb[j] = rows g and g + 8, halves 0 and 1, of the j-th unit in flight
+    uint4 wb[D][4];
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    auto load_unit = [&](int j, int i) {
+        const int64_t off = static_cast<int64_t>(warp + kRegWarps * i) * kUnitBytes;
+        wb[j][0] = lo_ok ? ldg_weights(wlo + off, policy) : zero;
+        wb[j][1] = lo_ok ? ldg_weights(wlo + off + 64, policy) : zero;
+        wb[j][2] = hi_ok ? ldg_weights(whi + off, policy) : zero;
+        wb[j][3] = hi_ok ? ldg_weights(whi + off + 64, policy) : zero;
+    };
+#pragma unroll
+    for (int j = 0; j < D; ++j)
+        if (j < nu) load_unit(j, j);
+
+    const uint32_t xs = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bar = smem_u32(&xfull);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
+    // The activations are written by the previous kernel on the stream.
+    griddep_wait();
+    const bool x_issued = a.skip_stage != 0;  // test hook: stage 0 of this kernel is its token copy
+    if (tid == 0 && x_issued) {
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(a.units_total * a.M * kUnitBytes));
+        tma_load_3d(xs, &tmap_x, 0, 0, 0, bar);
+    }
+    // Weights of later kernels named by the caller: into L2, after this CTA's own requests.
+    if (warp == kRegWarps - 1 && a.prefetch.count > 0)
+        prefetch_ranges_l2(a.prefetch, blockIdx.x, gridDim.x, lane);
+
+    bool ok = reg_wait(bar, 0u, a.wait_limit_ns);
+    if (!ok && lane == 0) {
+        atomicCAS(a.err_word, 0, kDeviceErrTimeout);
+        abort_flag = 1;
+    }
+
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (ok) {
+        const int gx = min(g, a.M - 1);
+        for (int i0 = 0; i0 < nu; i0 += D) {
+#pragma unroll
+            for (int j = 0; j < D; ++j) {
+                const int i = i0 + j;
+                if (i < nu) {
+                    const int L = (warp + kRegWarps * i) * a.M + gx;  // token line of this unit
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 lo = wb[j][h], hi = wb[j][2 + h];
+                        const uint4 xv = lds128u(xs + static_cast<uint32_t>(L * kUnitBytes) +
+                                                 static_cast<uint32_t>(((h * 4 + q) ^ (L & 7)) << 4));
+                        const uint32_t a0[4] = {lo.x, hi.x, lo.y, hi.y};
+                        const uint32_t a1[4] = {lo.z, hi.z, lo.w, hi.w};
+                        mma_bf16_16816(acc[0], a0, xv.x, xv.y);
+                        mma_bf16_16816(acc[1], a1, xv.z, xv.w);
+                    }
+                    if (i + D < nu) load_unit(j, i + D);
+                }
+            }
+        }
+    }
+
+    // ---- warp partials -> part[warp][slot][token]; C fragment rows g, g + 8, tokens 2q, 2q + 1 ----
+    part[warp][g][2 * q] = acc[0][0] + acc[1][0];
+    part[warp][g][2 * q + 1] = acc[0][1] + acc[1][1];
+    part[warp][g + 8][2 * q] = acc[0][2] + acc[1][2];
+    part[warp][g + 8][2 * q + 1] = acc[0][3] + acc[1][3];
+    __syncthreads();
+    const bool aborted = abort_flag != 0;
+
+    bool stored = false;
+    if (!aborted) {
+        for (int e = tid; e < rows_here * a.M; e += kRegThreads) {
+            const int tok = e / rows_here, slot = e - tok * rows_here;
+            float v = part[0][slot][tok];
+#pragma unroll
+            for (int w = 1; w < kRegWarps; ++w) v += part[w][slot][tok];
+            const int n = row0 + slot;
+            const int i = split_of(a.splits, n);
+            if (NORM && n - a.splits.off[i] < a.norm.cols[i]) {
+                // normalized column: parked in fp32 for the split's last CTA
+                a.norm.vals[a.norm.vals_off[i] + static_cast<int64_t>(tok) * a.norm.cols[i] + (n - a.splits.off[i])] = v;
+                sums[slot * 8 + tok] = v;
+            } else {
+                char *o = static_cast<char *>(a.splits.out[i]) +
+                          (static_cast<int64_t>(tok) * a.splits.rows[i] + (n - a.splits.off[i])) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(o) = __float2bfloat16_rn(v);
+                stored = true;
+            }
+        }
+    }
+    if constexpr (NORM) stored |= norm_epilogue<true, kRegMaxRows, 8>(a, sums, finish, row0, rows_here, aborted, tid);
+
+    if (aborted && tid == 0 && x_issued) {
+        // the token copy may still be in flight: let it land before the CTA leaves
+        const uint64_t t0 = global_timer_ns(), limit = a.wait_limit_ns / 16 + 1;
+        while (!mbar_try_wait(bar, 0u) && global_timer_ns() - t0 < limit) {
+        }
+    }
+    // Trigger the dependent launch only after every output store of this CTA is
+    // performed: each storing thread fences, then the CTA synchronises.
+    if (stored) fence_release_gpu();
+    __syncthreads();
+    griddep_launch_dependents();
+}
+
+}  // namespace hsp

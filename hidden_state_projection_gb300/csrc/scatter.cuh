@@ -19,11 +19,13 @@ struct OutRow {
     int64_t stride_bytes;
 };
 
-// The split that row n of the launch belongs to.
+// The split that row n of the launch belongs to: the number of later splits whose
+// first row is at or below n.  Every table entry is read at a constant index (no
+// dynamic indexing into the kernel parameters, no loop-carried dependence).
 __device__ __forceinline__ int split_of(const SplitTable &s, int n) {
     int i = 0;
-#pragma unroll 1
-    while (i + 1 < s.count && n >= s.off[i + 1]) ++i;
+#pragma unroll
+    for (int j = 1; j < kMaxSplits; ++j) i += (j < s.count && n >= s.off[j]) ? 1 : 0;
     return i;
 }
 

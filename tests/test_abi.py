@@ -114,7 +114,11 @@ def test_plan_fits_the_hardware(hsp):
                     assert p["smem_bytes"] <= 232448
                     assert p["row_ctas"] * p["rows_per_cta"] >= n
                     assert p["slices"] in (1, 2, 4, 8, 16)
-                    if p["engine"] == 0:     # bulk-copy + mma.sync / FMA kernel
+                    if p["engine"] == 2:     # register-ring kernel: bf16, M <= 8, 16 warps split K
+                        assert M <= 8 and dt == 0 and wl.K * 2 % 128 == 0
+                        assert p["rows_per_cta"] <= 16 and p["threads"] == 512 and p["slices"] == 1
+                        assert p["smem_bytes"] == wl.K * 2 * M + 1024
+                    elif p["engine"] == 0:   # bulk-copy + mma.sync / FMA kernel
                         assert p["rows_per_cta"] <= p["row_warps"] * p["row_tiles"] * 16
                         assert p["ring_stages"] >= 1
                         assert (p["row_warps"] * p["row_tiles"] * 16) % p["slices"] == 0
@@ -135,12 +139,14 @@ def test_pack_check_and_options(hsp):
     assert lib.proj_pack_check(base, base, 1280, 513, 1792, K, 0) == 0
     hsp.set_options(pdl=False, wait_limit_us=5, skip_stage=3)
     assert hsp.get_options() == {"pdl": 0, "wait_limit_us": 5, "skip_stage_plus1": 4,
-                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0, "small_m_path": 0}
+                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0, "small_m_path": 0,
+                                 "reg_path": 0}
     hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None, large_m_path=1, l2_prefetch=True)
     assert hsp.get_options()["large_m_path"] == 1 and hsp.get_options()["l2_prefetch"] == 1
     hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None)
     assert hsp.get_options() == {"pdl": 1, "wait_limit_us": 0, "skip_stage_plus1": 0,
-                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0, "small_m_path": 0}
+                                 "large_m_path": 0, "l2_prefetch": 0, "trigger_early": 0, "small_m_path": 0,
+                                 "reg_path": 0}
     with pytest.raises(hsp.ProjError):
         hsp.set_options(wait_limit_us=-1)
     with pytest.raises(hsp.ProjError):
@@ -149,6 +155,19 @@ def test_pack_check_and_options(hsp):
     assert [hsp.describe_plan(M, 7168, 2304, 0)["engine"] for M in (1, 8, 9, 16, 17, 64)] == [0, 0, 0, 0, 1, 1]
     hsp.set_options(large_m_path=2)
     assert [hsp.describe_plan(M, 7168, 2304, 0)["engine"] for M in (8, 9, 16, 17)] == [0, 1, 1, 1]
+    # bf16 rows of at most 80 k-units (K <= 5120) at M <= 8: the register-ring kernel
+    hsp.set_options(pdl=True)
+    assert [hsp.describe_plan(M, 5120, 1792, 0)["engine"] for M in (1, 4, 8, 9)] == [2, 2, 2, 0]
+    assert hsp.describe_plan(8, 5120, 1792, 0)["rows_per_cta"] <= 16
+    assert hsp.describe_plan(8, 5112, 1792, 0)["engine"] == 0        # rows not a whole number of k-units
+    assert hsp.describe_plan(1, 5120, 1792, 1)["engine"] == 0        # fp32
+    hsp.set_options(reg_path=1)
+    assert hsp.describe_plan(8, 5120, 1792, 0)["engine"] == 0
+    hsp.set_options(reg_path=2)
+    assert hsp.describe_plan(8, 7168, 2304, 0)["engine"] == 2
+    assert hsp.describe_plan(8, 8256, 2304, 0)["engine"] == 0        # 129 k-units: past the forced limit
+    with pytest.raises(hsp.ProjError):
+        hsp.set_options(reg_path=3)
     hsp.set_options(pdl=True)
 
 

@@ -168,3 +168,22 @@ def test_bf16_fma_small_m_path_matches_oracle(hsp, M):
     finally:
         hsp.set_options(pdl=True, small_m_path=0)
     check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"bf16 fma M{M}")
+
+
+@pytest.mark.parametrize("K,splits", [(5120, (1280, 512)), (1536, (200, 56)), (7168, (1536, 576, 128, 64))])
+@pytest.mark.parametrize("reg_path", [0, 1, 2])
+def test_register_ring_and_streaming_engines_match_oracle(hsp, K, splits, reg_path):
+    """bf16 at M <= 8: the register-ring kernel (default for K <= 5120, forced up to
+    K = 8192 with reg_path 2, where its ring of five k-units is refilled) and the
+    streaming kernel (reg_path 1) both agree with the oracle, fused and separate."""
+    hsp.set_options(pdl=True, reg_path=reg_path)
+    try:
+        for M in (1, 2, 5, 8):
+            x, ws = W.random_case(K, splits, M, "bf16", seed=1300 + M + K)
+            w_cat = torch.cat(ws, 0)
+            want = 2 if (reg_path == 2 or (reg_path == 0 and K <= 5120)) else 0
+            assert hsp.describe_plan(M, K, sum(splits), 0)["engine"] == want
+            outs = _run_both(hsp, x, w_cat, splits)
+            check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"reg_path {reg_path} K{K} M{M}")
+    finally:
+        hsp.set_options(pdl=True, reg_path=0)
