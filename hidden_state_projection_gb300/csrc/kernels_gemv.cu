@@ -1,0 +1,44 @@
+// kernels_gemv.cu -- the fp32 register GEMV kernel and its launch.
+#include <atomic>
+
+#include "gemv_kernel.cuh"
+#include "launch.h"
+
+namespace hsp {
+
+cudaError_t launch_gemv(const GemvLaunchReq &r) {
+    auto kern = hsp_gemv_kernel;
+    constexpr int kMaxDev = 64;
+    static std::atomic<unsigned char> configured[kMaxDev];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    if (!configured[dev].load(std::memory_order_acquire)) {
+        // the opt-in limit covers static and dynamic shared memory together
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 232448 - static_cast<int>(fa.sharedSizeBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev].store(1, std::memory_order_release);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = r.grid;
+    cfg.blockDim = dim3(kGemvThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(r.smem_bytes);
+    cfg.stream = r.stream;
+    cudaLaunchAttribute attrs[1];
+    unsigned n = 0;
+    if (r.pdl) {
+        attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, r.args);
+}
+
+}  // namespace hsp

@@ -55,6 +55,18 @@ cudaError_t launch_reg(const RegLaunchReq &r);
 constexpr int kRegThreadsHost = 16 * 32;
 constexpr int kRegDepthHost = 5;
 
+// fp32 register GEMV launch (PROJ_FP32, M <= 8, K <= 8192, M * K * 4 <= kGemvMaxTokenBytes).
+struct GemvLaunchReq {
+    dim3 grid;       // (row CTAs, 1, 1)
+    int smem_bytes;  // the tokens: M * K * 4
+    int pdl;
+    cudaStream_t stream;
+    StreamArgs args;  // w, x, row_bytes, n_rows, rows_per_cta, M, hooks, splits, prefetch
+};
+cudaError_t launch_gemv(const GemvLaunchReq &r);
+constexpr int kGemvThreadsHost = 16 * 32;
+constexpr int kGemvMaxTokenBytes = 192 * 1024;
+
 // Threads per CTA of a bucket (eight consumer warps + one producer warp).
 constexpr int kThreadsPerCta = 9 * 32;
 constexpr int kUmmaThreadsHost = 128;

@@ -10,7 +10,8 @@
 //   bucket 2, 33 <= M <= 64: 8 token tiles; 4 row warps x 2 K warps, S K slices
 // bf16 with M <= 8 and rows of at most 80 k-units of 128 bytes (K <= 5120) runs the
 // register-ring kernel instead (sixteen warps split K, weights straight into
-// registers), measured faster on GB300 there.
+// registers), and fp32 with M <= 8 the register GEMV kernel (no K slices), both
+// measured faster on GB300 there.
 // The K-split (warps WK, slices S, box width) is a function of (K, dtype,
 // bucket) only, so an output row is summed in the same order whatever the
 // number of rows in the launch -- the property that makes the fused and the
@@ -638,12 +639,91 @@ proj_status launch_reg_rows(const DeviceInfo &dev, const void *x, const void *w,
     return PROJ_OK;
 }
 
+// ---- fp32 register GEMV plan (PROJ_FP32, M <= 8) ------------------------------
+
+// PROJ_FP32 with M <= 8, K <= 8192 and the tokens within 192 KB of shared memory runs
+// the register GEMV kernel: one CTA per ceil(N / SMs) rows and all of K, no clusters
+// (measured on GB300: indexer wk ++ weights_proj 192 x 7168 and the GLM router 256 x 6144;
+// numbers in the design notes).  Option reg_path 1 turns it off.  The choice depends on
+// (M, K, dtype) only.
+bool use_gemv(int M, int K, proj_dtype dt) {
+    if (dt != PROJ_FP32 || M < 1 || M > 8 || K > 8192) return false;
+    if (g_opt_reg_path.load() == 1) return false;
+    return static_cast<int64_t>(M) * K * 4 <= hsp::kGemvMaxTokenBytes;
+}
+
+struct GemvPlan {
+    int R, grid, smem;
+};
+
+void make_gemv_plan(int M, int K, int n_rows, int sms, GemvPlan *p) {
+    p->R = std::max(1, ceil_div(n_rows, std::max(1, sms)));
+    p->grid = ceil_div(n_rows, p->R);
+    p->smem = M * K * 4;
+}
+
+void gemv_plan_info(int M, int K, const GemvPlan &p, proj_plan_info *i) {
+    memset(i, 0, sizeof *i);
+    i->bucket = 0;
+    i->compute = hsp::kFmaFp32;
+    i->rows_per_cta = p.R;
+    i->row_ctas = p.grid;
+    i->slices = 1;
+    i->k_warps = 16;
+    i->row_warps = 1;
+    i->row_tiles = 1;
+    i->token_tiles = 1;
+    i->ring_stages = 2;  // row blocks in flight
+    i->stage_bytes = 0;
+    i->smem_bytes = p.smem;
+    i->k_per_stage = K;
+    i->stages_total = ceil_div(p.R, 2);  // row blocks of two rows
+    i->threads = hsp::kGemvThreadsHost;
+    i->units_per_slice = ceil_div(K * 4, hsp::kUnitBytes);
+    i->engine = 3;
+    i->tensor_copies = 0;  // the tokens arrive as one 1-D bulk copy
+    (void)M;
+}
+
+proj_status launch_gemv_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
+                             const hsp::SplitTable &splits, const hsp::PrefetchList &pf, cudaStream_t stream) {
+    GemvPlan p;
+    make_gemv_plan(M, K, n_rows, dev.sms, &p);
+    hsp::GemvLaunchReq r{};
+    r.grid = dim3(static_cast<unsigned>(p.grid), 1, 1);
+    r.smem_bytes = p.smem;
+    r.pdl = g_opt_pdl.load();
+    r.stream = stream;
+    StreamArgs &a = r.args;
+    a.w = static_cast<const char *>(w);
+    a.x = static_cast<const char *>(x);
+    a.row_bytes = static_cast<int64_t>(K) * 4;
+    a.n_rows = n_rows;
+    a.rows_per_cta = p.R;
+    a.M = M;
+    a.units_total = ceil_div(K * 4, hsp::kUnitBytes);
+    a.units_per_slice = a.units_total;
+    a.slices = 1;
+    a.skip_stage = g_opt_skip_stage_plus1.load() - 1;
+    a.trigger_early = g_opt_trigger_early.load();
+    const int wus = g_opt_wait_us.load();
+    a.wait_limit_ns = wus > 0 ? static_cast<uint64_t>(wus) * 1000ull : kDefaultWaitNs;
+    a.err_word = dev.err_word;
+    a.splits = splits;
+    a.prefetch = pf;
+    cudaError_t e = hsp::launch_gemv(r);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch (fp32 register GEMV path)");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return PROJ_OK;
+}
+
 // One launch over `n_rows` weight rows starting at `w` (already offset to the first row).
 proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int n_rows, int M, int K,
                         proj_dtype dt, const hsp::SplitTable &splits, const hsp::PrefetchList &pf,
                         cudaStream_t stream, const hsp::NormArgs *norm = nullptr) {
     if (use_umma(M, dt)) return launch_umma_rows(dev, x, w, n_rows, M, K, dt, splits, pf, stream);
     if (use_reg(M, K, dt)) return launch_reg_rows(dev, x, w, n_rows, M, K, splits, pf, stream, norm);
+    if (use_gemv(M, K, dt)) return launch_gemv_rows(dev, x, w, n_rows, M, K, splits, pf, stream);
     Plan p;
     make_plan(M, K, n_rows, dt, dev.cluster_ctas, &p);
     if (p.ring_stages < 1 || p.smem > kSmemLimit)
@@ -1007,6 +1087,12 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
         RegPlan rp;
         make_reg_plan(M, K, n_rows, ctas[1], &rp);
         reg_plan_info(M, K, rp, info);
+        return ok();
+    }
+    if (use_gemv(M, K, dtype)) {
+        GemvPlan gp;
+        make_gemv_plan(M, K, n_rows, ctas[1], &gp);
+        gemv_plan_info(M, K, gp, info);
         return ok();
     }
     Plan p;

@@ -114,7 +114,10 @@ def test_plan_fits_the_hardware(hsp):
                     assert p["smem_bytes"] <= 232448
                     assert p["row_ctas"] * p["rows_per_cta"] >= n
                     assert p["slices"] in (1, 2, 4, 8, 16)
-                    if p["engine"] == 2:     # register-ring kernel: bf16, M <= 8, 16 warps split K
+                    if p["engine"] == 3:     # fp32 register GEMV: M <= 8, all of K per CTA
+                        assert M <= 8 and dt == 1 and p["slices"] == 1 and p["threads"] == 512
+                        assert p["smem_bytes"] == M * wl.K * 4 <= 192 * 1024
+                    elif p["engine"] == 2:   # register-ring kernel: bf16, M <= 8, 16 warps split K
                         assert M <= 8 and dt == 0 and wl.K * 2 % 128 == 0
                         assert p["rows_per_cta"] <= 16 and p["threads"] == 512 and p["slices"] == 1
                         assert p["smem_bytes"] == wl.K * 2 * M + 1024
@@ -160,12 +163,20 @@ def test_pack_check_and_options(hsp):
     assert [hsp.describe_plan(M, 5120, 1792, 0)["engine"] for M in (1, 4, 8, 9)] == [2, 2, 2, 0]
     assert hsp.describe_plan(8, 5120, 1792, 0)["rows_per_cta"] <= 16
     assert hsp.describe_plan(8, 5112, 1792, 0)["engine"] == 0        # rows not a whole number of k-units
-    assert hsp.describe_plan(1, 5120, 1792, 1)["engine"] == 0        # fp32
+    assert hsp.describe_plan(1, 5120, 1792, 1)["engine"] == 3        # fp32: the register GEMV
     hsp.set_options(reg_path=1)
     assert hsp.describe_plan(8, 5120, 1792, 0)["engine"] == 0
     hsp.set_options(reg_path=2)
     assert hsp.describe_plan(8, 7168, 2304, 0)["engine"] == 2
     assert hsp.describe_plan(8, 8256, 2304, 0)["engine"] == 0        # 129 k-units: past the forced limit
+    # fp32 at M <= 8 with the tokens within 192 KB: the register GEMV; tf32 keeps the tensor cores
+    hsp.set_options(pdl=True)
+    assert [hsp.describe_plan(M, 7168, 192, 1)["engine"] for M in (1, 4, 6, 7, 9)] == [3, 3, 3, 0, 0]
+    assert [hsp.describe_plan(M, 6144, 256, 1)["engine"] for M in (1, 8)] == [3, 3]
+    assert hsp.describe_plan(1, 7168, 192, 2)["engine"] == 0
+    assert hsp.describe_plan(1, 8196, 192, 1)["engine"] == 0            # K past 8192
+    hsp.set_options(reg_path=1)
+    assert hsp.describe_plan(1, 7168, 192, 1)["engine"] == 0
     with pytest.raises(hsp.ProjError):
         hsp.set_options(reg_path=3)
     hsp.set_options(pdl=True)

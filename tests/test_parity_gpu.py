@@ -187,3 +187,23 @@ def test_register_ring_and_streaming_engines_match_oracle(hsp, K, splits, reg_pa
             check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"reg_path {reg_path} K{K} M{M}")
     finally:
         hsp.set_options(pdl=True, reg_path=0)
+
+
+@pytest.mark.parametrize("K,splits", [(7168, (128, 64)), (6144, (256,)), (1536, (200, 56)), (4096, (5000,))])
+@pytest.mark.parametrize("reg_path", [0, 1])
+def test_fp32_register_gemv_and_streaming_match_oracle(hsp, K, splits, reg_path):
+    """fp32 at M <= 8: the register GEMV kernel (default; rows in blocks of two, all of K
+    per CTA, 5000 rows = 33 rows per CTA exercises the block loop) and the streaming
+    kernel (reg_path 1) both meet the fp32 tolerance, fused and separate."""
+    hsp.set_options(pdl=True, reg_path=reg_path)
+    try:
+        for M in (1, 3, 4, 8):
+            if M * K * 4 > 192 * 1024 and reg_path == 0:
+                continue
+            x, ws = W.random_case(K, splits, M, "fp32", seed=1700 + M + K)
+            w_cat = torch.cat(ws, 0)
+            assert hsp.describe_plan(M, K, sum(splits), 1)["engine"] == (3 if reg_path == 0 else 0)
+            outs = _run_both(hsp, x, w_cat, splits)
+            check_close(outs, oracle_outputs(x, w_cat, splits), "fp32", f"reg_path {reg_path} K{K} M{M}")
+    finally:
+        hsp.set_options(pdl=True, reg_path=0)
