@@ -30,7 +30,8 @@ STATUS = {v: k for k, v in STATUS_NAMES.items()}
 MAX_SPLITS = 8
 MAX_M = 64
 
-EXPORTED = ("proj_fused_gemm", "proj_fused_gemm_prefetch", "proj_fused_gemm_rmsnorm", "proj_rmsnorm_workspace_bytes",
+EXPORTED = ("proj_fused_gemm", "proj_fused_gemm_prefetch", "proj_fused_gemm_host",
+            "proj_host_plan_create", "proj_host_plan_launch", "proj_host_plan_destroy", "proj_fused_gemm_rmsnorm", "proj_rmsnorm_workspace_bytes",
             "proj_fused_gemm_rmsnorm_static",
             "proj_separate_gemm", "proj_pack_weights", "proj_pack_check",
             "proj_supported", "proj_describe_plan", "proj_set_options", "proj_get_options",
@@ -82,6 +83,14 @@ def lib() -> ctypes.CDLL:
     for name in ("proj_fused_gemm", "proj_separate_gemm"):
         getattr(L, name).argtypes = gemm_args
         getattr(L, name).restype = ctypes.c_int
+    L.proj_fused_gemm_host.argtypes = gemm_args[:8] + [vp, ctypes.POINTER(vp), vp]
+    L.proj_fused_gemm_host.restype = ctypes.c_int
+    L.proj_host_plan_create.argtypes = gemm_args[:8] + [vp, ctypes.POINTER(vp), ctypes.POINTER(vp)]
+    L.proj_host_plan_create.restype = ctypes.c_int
+    L.proj_host_plan_launch.argtypes = [vp, vp]
+    L.proj_host_plan_launch.restype = ctypes.c_int
+    L.proj_host_plan_destroy.argtypes = [vp]
+    L.proj_host_plan_destroy.restype = ctypes.c_int
     L.proj_fused_gemm_prefetch.argtypes = gemm_args[:8] + [ctypes.POINTER(PrefetchRange), i32, vp]
     L.proj_fused_gemm_prefetch.restype = ctypes.c_int
     L.proj_pack_weights.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(i32), i32, i32, ctypes.c_int, vp, vp]
@@ -207,6 +216,81 @@ def fused_gemm_prefetch(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[i
     def fn(xp, wp, sp, op, M, K, dt, st):
         fused_gemm_prefetch_ptr(xp, wp, sp, op, M, K, dt, ranges, st)
     return _gemm(fn, x, w_cat, splits, outs, tf32, stream)
+
+
+class HostCall:
+    """A fused call bound once to fixed buffers, for a loop that repeats it (a decode
+    step): proj_fused_gemm_host with its ctypes arguments built here, so each call is one
+    foreign-function call.  x_host / outs_host are pinned CPU tensors, x_dev / outs_dev
+    device staging tensors of the same shapes; w_cat stays on the device.  Calling the
+    object enqueues H2D copy, projection and D2H copies on the stream; synchronise before
+    reading outs_host."""
+
+    def __init__(self, x_host: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
+                 outs_host: Sequence[torch.Tensor], x_dev: torch.Tensor, outs_dev: Sequence[torch.Tensor],
+                 tf32: bool = False, stream=None):
+        M, K = x_dev.shape
+        if x_host.shape != x_dev.shape or x_host.dtype != x_dev.dtype or not x_host.is_contiguous():
+            raise ProjError(1, "x_host must be a dense tensor shaped and typed like x_dev")
+        if len(outs_host) != len(splits) or len(outs_dev) != len(splits):
+            raise ProjError(1, "one host and one device output per split")
+        _outs(x_dev, splits, list(outs_dev))
+        for h, n in zip(outs_host, splits):
+            if h.shape != (M, int(n)) or h.dtype != x_dev.dtype or not h.is_contiguous():
+                raise ProjError(1, f"host output must be a dense [{M}, {n}] {x_dev.dtype} tensor")
+        self._keep = (x_host, w_cat, list(outs_host), x_dev, list(outs_dev))
+        vp = ctypes.c_void_p
+        self._args = (x_host.data_ptr(), w_cat.data_ptr(),
+                      (ctypes.c_int32 * len(splits))(*[int(s) for s in splits]), len(splits),
+                      (vp * len(splits))(*[h.data_ptr() for h in outs_host]), M, K, dtype_code(x_dev, tf32),
+                      x_dev.data_ptr(), (vp * len(splits))(*[o.data_ptr() for o in outs_dev]), _stream_ptr(stream))
+        self._fn = lib().proj_fused_gemm_host
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != 0:
+            _check(rc)
+
+
+class HostPlan:
+    """proj_host_plan_*: the host step of HostCall recorded once as a CUDA graph inside the
+    library; each call is one graph launch (H2D copy, projection, D2H copies) on the
+    stream.  x_host and outs_host must be pinned; all buffers are kept alive by the plan."""
+
+    def __init__(self, x_host: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
+                 outs_host: Sequence[torch.Tensor], x_dev: torch.Tensor, outs_dev: Sequence[torch.Tensor],
+                 tf32: bool = False, stream=None):
+        bound = HostCall(x_host, w_cat, splits, outs_host, x_dev, outs_dev, tf32, stream)
+        self._keep = bound._keep
+        a = bound._args
+        self._handle = ctypes.c_void_p()
+        _check(lib().proj_host_plan_create(*a[:10], ctypes.byref(self._handle)))
+        self._stream = _stream_ptr(stream)
+        self._launch = lib().proj_host_plan_launch
+
+    def __call__(self) -> None:
+        rc = self._launch(self._handle, self._stream)
+        if rc != 0:
+            _check(rc)
+
+    def close(self) -> None:
+        if self._handle:
+            _check(lib().proj_host_plan_destroy(self._handle))
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            if self._handle and _lib is not None:
+                _lib.proj_host_plan_destroy(self._handle)
+        except Exception:
+            pass
+
+
+def fused_gemm_host(x_host: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
+                    outs_host: Sequence[torch.Tensor], x_dev: torch.Tensor, outs_dev: Sequence[torch.Tensor],
+                    tf32: bool = False, stream=None) -> None:
+    """One proj_fused_gemm_host call (see HostCall for a loop of them)."""
+    HostCall(x_host, w_cat, splits, outs_host, x_dev, outs_dev, tf32, stream)()
 
 
 def rmsnorm_workspace_bytes(M: int, K: int, splits: Sequence[int], norm_cols: Sequence[int], dtype: int = 0) -> int:

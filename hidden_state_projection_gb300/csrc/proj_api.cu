@@ -924,6 +924,12 @@ proj_status norm_layout(int32_t M, int32_t K, const int32_t *n_splits, int32_t n
 
 }  // namespace
 
+// A recorded host step (proj_host_plan_create): the graph and its executable.
+struct proj_host_plan {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
 extern "C" {
 
 size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_splits, int32_t num_splits,
@@ -1005,6 +1011,114 @@ proj_status proj_fused_gemm_prefetch(const void *x, const void *w_cat, const int
         ++pf.count;
     }
     return fused_impl(x, w_cat, n_splits, num_splits, outs, M, K, dtype, pf, stream);
+}
+
+proj_status proj_fused_gemm_host(const void *x_host, const void *w_cat, const int32_t *n_splits,
+                                 int32_t num_splits, void *const *outs_host, int32_t M, int32_t K, proj_dtype dtype,
+                                 void *x_dev, void *const *outs_dev, proj_stream_t stream) {
+    int64_t n_total = 0;
+    proj_status st = validate(x_dev, w_cat, n_splits, num_splits, outs_dev, M, K, dtype, &n_total);
+    if (st != PROJ_OK) return st;
+    if (M == 0) return ok();
+    if (!x_host || !outs_host) return fail(PROJ_ERR_INVALID_ARG, "x_host and outs_host must not be NULL");
+    for (int i = 0; i < num_splits; ++i)
+        if (!outs_host[i]) return fail(PROJ_ERR_INVALID_ARG, "outs_host[%d] is NULL", i);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t esz = static_cast<size_t>(elem_size(dtype));
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, static_cast<size_t>(M) * K * esz, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (tokens to the device)");
+    // An output in page-locked host memory that the device can address (mapped, as
+    // cudaHostAlloc memory is under unified addressing) is written by the kernel itself,
+    // over the host link, instead of through a staging buffer and a copy; the stream's
+    // completion makes those stores visible to the host like a copy's.
+    void *direct[PROJ_MAX_SPLITS];
+    for (int i = 0; i < num_splits; ++i) {
+        direct[i] = nullptr;
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, outs_host[i]) == cudaSuccess) {
+            if (pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+                (reinterpret_cast<uintptr_t>(pa.devicePointer) & (esz - 1)) == 0)
+                direct[i] = pa.devicePointer;
+        } else {
+            (void)cudaGetLastError();  // pageable memory: not an error, copy it
+        }
+    }
+    void *kout[PROJ_MAX_SPLITS];
+    for (int i = 0; i < num_splits; ++i) kout[i] = direct[i] ? direct[i] : outs_dev[i];
+    hsp::PrefetchList none;
+    memset(&none, 0, sizeof none);
+    st = fused_impl(x_dev, w_cat, n_splits, num_splits, kout, M, K, dtype, none, stream);
+    if (st != PROJ_OK) return st;
+    for (int i = 0; i < num_splits; ++i) {
+        if (direct[i]) continue;
+        e = cudaMemcpyAsync(outs_host[i], outs_dev[i], static_cast<size_t>(M) * n_splits[i] * esz,
+                            cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (outputs to the host)");
+    }
+    return ok();
+}
+
+proj_status proj_host_plan_create(const void *x_host, const void *w_cat, const int32_t *n_splits,
+                                  int32_t num_splits, void *const *outs_host, int32_t M, int32_t K, proj_dtype dtype,
+                                  void *x_dev, void *const *outs_dev, proj_host_plan **plan) {
+    if (!plan) return fail(PROJ_ERR_INVALID_ARG, "plan must not be NULL");
+    *plan = nullptr;
+    int64_t n_total = 0;
+    proj_status st = validate(x_dev, w_cat, n_splits, num_splits, outs_dev, M, K, dtype, &n_total);
+    if (st != PROJ_OK) return st;
+    if (M == 0) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "a host plan needs M >= 1");
+    DeviceInfo dev;
+    if ((st = device_info(&dev)) != PROJ_OK) return st;
+    cudaStream_t cs = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags (recording stream)");
+    proj_host_plan *p = new proj_host_plan;
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        st = proj_fused_gemm_host(x_host, w_cat, n_splits, num_splits, outs_host, M, K, dtype, x_dev, outs_dev,
+                                  reinterpret_cast<proj_stream_t>(cs));
+        cudaGraph_t g = nullptr;
+        const cudaError_t ee = cudaStreamEndCapture(cs, &g);
+        p->graph = g;
+        if (st == PROJ_OK && ee != cudaSuccess) st = cuda_fail(ee, "cudaStreamEndCapture");
+        if (st == PROJ_OK) {
+            e = cudaGraphInstantiate(&p->exec, p->graph, 0);
+            if (e != cudaSuccess) st = cuda_fail(e, "cudaGraphInstantiate");
+        }
+    } else {
+        st = cuda_fail(e, "cudaStreamBeginCapture");
+    }
+    (void)cudaStreamDestroy(cs);
+    if (st != PROJ_OK) {
+        char saved[sizeof g_last_error];
+        memcpy(saved, g_last_error, sizeof saved);
+        if (p->exec) (void)cudaGraphExecDestroy(p->exec);
+        if (p->graph) (void)cudaGraphDestroy(p->graph);
+        delete p;
+        (void)cudaGetLastError();
+        memcpy(g_last_error, saved, sizeof saved);
+        return st;
+    }
+    *plan = p;
+    return ok();
+}
+
+proj_status proj_host_plan_launch(proj_host_plan *plan, proj_stream_t stream) {
+    if (!plan || !plan->exec) return fail(PROJ_ERR_INVALID_ARG, "plan is NULL or not created");
+    const cudaError_t e = cudaGraphLaunch(plan->exec, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch (host plan)");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return ok();
+}
+
+proj_status proj_host_plan_destroy(proj_host_plan *plan) {
+    if (!plan) return ok();
+    cudaError_t e1 = plan->exec ? cudaGraphExecDestroy(plan->exec) : cudaSuccess;
+    cudaError_t e2 = plan->graph ? cudaGraphDestroy(plan->graph) : cudaSuccess;
+    delete plan;
+    if (e1 != cudaSuccess) return cuda_fail(e1, "cudaGraphExecDestroy");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "cudaGraphDestroy");
+    return ok();
 }
 
 proj_status proj_separate_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,

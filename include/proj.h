@@ -244,6 +244,51 @@ proj_status proj_fused_gemm_rmsnorm_static(const void *x, const void *w_cat, con
                                            int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream);
 
 /*
+ * proj_fused_gemm_host -- proj_fused_gemm for a caller whose tokens and results live in
+ * host memory (a decode step that receives the hidden state from the host and hands the
+ * projections back to it).  Enqueued on `stream`, in this order: one host-to-device copy
+ * of x_host into x_dev (M * K elements), the fused projection from x_dev into outs_dev
+ * (exactly proj_fused_gemm: same kernel, same bits), one device-to-host copy of each
+ * outs_dev[i] into outs_host[i].  An outs_host[i] in page-locked memory that the device
+ * can address (cudaHostAlloc memory under unified addressing) is instead written by the
+ * kernel directly, over the host link, and outs_dev[i] is left untouched.  The call
+ * returns once everything is enqueued; synchronise the stream before reading outs_host.
+ *   x_host     host [M, K]; page-locked (cudaHostAlloc / pinned) for the copies to be
+ *              asynchronous, pageable memory makes the copy synchronous
+ *   outs_host  host array of num_splits host pointers, outs_host[i] is [M, N_i]
+ *   x_dev      device [M, K] staging buffer, 16-byte aligned, owned by the caller
+ *   outs_dev   host array of num_splits device pointers, outs_dev[i] is [M, N_i]
+ * Other arguments, limits and errors as proj_fused_gemm; a failed copy returns
+ * PROJ_ERR_CUDA.  The library allocates nothing: both staging buffers are the caller's.
+ */
+proj_status proj_fused_gemm_host(const void *x_host, const void *w_cat, const int32_t *n_splits,
+                                 int32_t num_splits, void *const *outs_host, int32_t M, int32_t K,
+                                 proj_dtype dtype, void *x_dev, void *const *outs_dev,
+                                 proj_stream_t stream);
+
+/*
+ * Host plans -- proj_fused_gemm_host bound once to fixed buffers and recorded as one CUDA
+ * graph (the host-to-device copy, the fused projection, the device-to-host copies), so
+ * that a loop repeating the step (decode) costs one graph launch per step on the host.
+ * proj_host_plan_create takes the arguments of proj_fused_gemm_host (x_host and every
+ * outs_host[i] must be page-locked: the recording refuses pageable memory with
+ * PROJ_ERR_CUDA) and records the work with the options in force at that moment (PDL,
+ * engine switches).  The buffers must stay allocated until the plan is destroyed.
+ * proj_host_plan_launch enqueues one step on `stream` (same bits as proj_fused_gemm);
+ * synchronise the stream before reading the host outputs.  proj_host_plan_destroy
+ * releases the graph; NULL is accepted.  The plan is host state only: no device memory
+ * is allocated by the library.  A plan may be launched from one thread at a time.
+ */
+typedef struct proj_host_plan proj_host_plan;
+
+proj_status proj_host_plan_create(const void *x_host, const void *w_cat, const int32_t *n_splits,
+                                  int32_t num_splits, void *const *outs_host, int32_t M, int32_t K,
+                                  proj_dtype dtype, void *x_dev, void *const *outs_dev,
+                                  proj_host_plan **plan);
+proj_status proj_host_plan_launch(proj_host_plan *plan, proj_stream_t stream);
+proj_status proj_host_plan_destroy(proj_host_plan *plan);
+
+/*
  * proj_separate_gemm -- one launch per projection over its row range of the same
  * w_cat (TensorRT-LLM PR #20636, Description: "2-8 tokens: one tinygemm2 per
  * projection").  Same arguments and outputs as proj_fused_gemm, bitwise equal to it.

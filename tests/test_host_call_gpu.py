@@ -1,0 +1,104 @@
+"""proj_fused_gemm_host through the C ABI: tokens from pinned host memory, outputs back
+to host memory, the projection in between bitwise that of proj_fused_gemm; a bound call
+(HostCall) repeated over several inputs; NULL host pointers refused before anything is
+enqueued."""
+import ctypes
+
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hsp():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import hidden_state_projection_gb300 as m
+    m.lib()
+    m.set_options(pdl=True)
+    return m
+
+
+@pytest.mark.parametrize("name,M,tf32", [("wq_a_wkv", 8, False), ("wq_a_wkv_m1", 1, False), ("qk_indexer", 64, False),
+                                         ("indexer_fp32", 4, False), ("indexer_fp32", 4, True)])
+def test_host_call_matches_device_call(hsp, name, M, tf32):
+    wl = W.WORKLOADS[name]
+    w = W.weight_cat(wl).cuda()
+    x_dev = torch.empty((M, wl.K), dtype=w.dtype, device="cuda")
+    outs_dev = [torch.empty((M, n), dtype=w.dtype, device="cuda") for n in wl.splits]
+    outs_host = [torch.full((M, n), float("nan"), dtype=w.dtype).pin_memory() for n in wl.splits]
+    xs = [W.activation(wl, M, c).pin_memory() for c in range(3)]
+    calls = [hsp.HostCall(xh, w, wl.splits, outs_host, x_dev, outs_dev, tf32=tf32) for xh in xs]
+    for rep in range(2):                      # every bound call twice, in a row
+        for xh, call in zip(xs, calls):
+            call()
+            torch.cuda.synchronize()
+            ref = hsp.fused_gemm(xh.cuda(), w, wl.splits, tf32=tf32)
+            hsp.check_device_error()
+            for h, r in zip(outs_host, ref):
+                assert torch.equal(h, r.cpu()), (name, M, rep)
+
+
+def test_host_call_refuses_null_host_pointers(hsp):
+    S = hsp.STATUS
+    lib = hsp.lib()
+    x_dev = torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((24, 64), dtype=torch.bfloat16, device="cuda")
+    outs_dev = [torch.zeros((1, 16), dtype=torch.bfloat16, device="cuda"),
+                torch.zeros((1, 8), dtype=torch.bfloat16, device="cuda")]
+    host = [torch.zeros((1, 16), dtype=torch.bfloat16).pin_memory(), torch.zeros((1, 8), dtype=torch.bfloat16).pin_memory()]
+    ns = (ctypes.c_int32 * 2)(16, 8)
+    od = (ctypes.c_void_p * 2)(*[o.data_ptr() for o in outs_dev])
+    oh = (ctypes.c_void_p * 2)(host[0].data_ptr(), None)
+    xh = torch.zeros((1, 64), dtype=torch.bfloat16).pin_memory()
+    before = hsp.launch_count()
+    assert lib.proj_fused_gemm_host(None, w.data_ptr(), ns, 2, oh, 1, 64, 0, x_dev.data_ptr(), od, None) == \
+        S["PROJ_ERR_INVALID_ARG"]
+    assert lib.proj_fused_gemm_host(xh.data_ptr(), w.data_ptr(), ns, 2, oh, 1, 64, 0, x_dev.data_ptr(), od, None) == \
+        S["PROJ_ERR_INVALID_ARG"]
+    assert b"outs_host[1]" in lib.proj_last_error_string()
+    assert hsp.launch_count() == before
+
+
+@pytest.mark.parametrize("name,M", [("wq_a_wkv", 8), ("qk_indexer", 64), ("indexer_fp32", 4)])
+def test_host_plan_replays_match_device_call(hsp, name, M):
+    """A host plan (one recorded graph per bound step) gives the bits of fused_gemm on
+    every launch; two plans over the same staging buffers interleave correctly."""
+    wl = W.WORKLOADS[name]
+    ws = [W.weight_cat(wl, c).cuda() for c in range(2)]
+    x_dev = torch.empty((M, wl.K), dtype=ws[0].dtype, device="cuda")
+    outs_dev = [torch.empty((M, n), dtype=ws[0].dtype, device="cuda") for n in wl.splits]
+    outs_host = [torch.full((M, n), float("nan"), dtype=ws[0].dtype).pin_memory() for n in wl.splits]
+    xs = [W.activation(wl, M, c).pin_memory() for c in range(2)]
+    plans = [hsp.HostPlan(xs[c], ws[c], wl.splits, outs_host, x_dev, outs_dev) for c in range(2)]
+    try:
+        for rep in range(3):
+            for c in (0, 1):
+                plans[c]()
+                torch.cuda.synchronize()
+                ref = hsp.fused_gemm(xs[c].cuda(), ws[c], wl.splits)
+                hsp.check_device_error()
+                for h, r in zip(outs_host, ref):
+                    assert torch.equal(h, r.cpu()), (name, M, rep, c)
+    finally:
+        for p in plans:
+            p.close()
+
+
+def test_host_plan_argument_checks(hsp):
+    S = hsp.STATUS
+    lib = hsp.lib()
+    assert lib.proj_host_plan_launch(None, None) == S["PROJ_ERR_INVALID_ARG"]
+    assert lib.proj_host_plan_destroy(None) == 0
+    x_dev = torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((24, 64), dtype=torch.bfloat16, device="cuda")
+    ns = (ctypes.c_int32 * 2)(16, 8)
+    od = (ctypes.c_void_p * 2)(*[torch.zeros((1, n), dtype=torch.bfloat16, device="cuda").data_ptr() for n in (16, 8)])
+    oh = (ctypes.c_void_p * 2)(None, None)
+    h = ctypes.c_void_p()
+    assert lib.proj_host_plan_create(None, w.data_ptr(), ns, 2, oh, 1, 64, 0, x_dev.data_ptr(), od,
+                                     ctypes.byref(h)) == S["PROJ_ERR_INVALID_ARG"]
+    assert not h.value
