@@ -153,6 +153,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- multi-rank (replicas)
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the slowest replica sets the job's time).  The
+    tensor lives on `device`: CUDA under NCCL, the CPU under gloo."""
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_call(ms_per_step: float, calls_per_rank: int, world_size: int) -> float:
+    """Whole-job µs per call: world_size replicas each ran calls_per_rank calls inside one
+    step of ms_per_step (the max over ranks), so the job finished world_size * calls_per_rank
+    calls in that time (weak scaling: per-GPU work fixed as N grows)."""
+    return ms_per_step * 1000.0 / (calls_per_rank * world_size)
+
+
 # ---------------------------------------------------------------- our arm
 
 class Setup:
@@ -309,15 +327,12 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         total_ms, per = time_graph(g, args.steps, args.warmup, barrier)
     hsp.check_device_error()
-    ms_per_step = total_ms / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    us_call = ms_per_step * 1000.0 / args.calls
+    ms_per_step = max_over_ranks(total_ms / args.steps, dev) if ws > 1 else total_ms / args.steps
+    # whole job: every rank ran args.calls calls per step, all within ms_per_step
+    us_call = job_us_per_call(ms_per_step, args.calls, ws)
     bytes_call = st.bytes_per_call()
-    achieved = bytes_call / (us_call * 1e-6) / 1e9
+    # roofline of one GPU's kernel: its own calls in the (max over ranks) step time
+    achieved = bytes_call / (ms_per_step * 1000.0 / args.calls * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
     e2e_us, h2d, d2h, e2e_plan_us = time_e2e(hsp, st, args.e2e_calls)
     # Same calls, each also prefetching the next call's weights into L2 (the cross-kernel
@@ -355,7 +370,7 @@ def run_ours(args):
                      "traffic": args.traffic if args.traffic is not None else profiled_traffic(name, M),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
-                     "bytes_per_call": bytes_call, "us_per_call": round(us_call, 4)},
+                     "bytes_per_call": bytes_call, "us_per_call_per_gpu": round(ms_per_step * 1000.0 / args.calls, 4)},
         "e2e": {"value": round(e2e_us, 3), "unit": "µs/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "public API proj_fused_gemm_host per step (bound HostCall): H2D copy of x from pinned memory, fused call, outputs stored by the kernel into pinned mapped host memory",
@@ -368,7 +383,7 @@ def run_ours(args):
         "clocks": clocks,
         "step_ms_min": round(min(per), 5), "step_ms_median": round(statistics.median(per), 5),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, M, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
