@@ -269,29 +269,38 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
         // holding about kStageWeightBytes of weights.  One weight box and one token
         // box per stage, each rounded up to 1024 bytes.
         auto box = [](int rows, int su) { return ceil_div(rows * su * hsp::kUnitBytes, 1024) * 1024; };
-        const int target = std::max(1, kStageWeightBytes / (p->R * hsp::kUnitBytes));
-        // the divisor of the slice nearest the target (the larger one on a tie), at
-        // most half the slice: at least two stages, so loads and products overlap
-        int su = 0;
-        for (int d = 1; d <= std::max(1, Us / 2); ++d)
-            if (Us % d == 0 && (su == 0 || std::abs(d - target) <= std::abs(su - target))) su = d;
-        for (;;) {
-            const int stage = box(p->R, su) + box(M, su);
-            const int nst = ceil_div(Us, su);
-            int ring = std::min(std::min(nst, budget / stage), kMaxRingStages);
-            if (ring >= std::min(2, nst) || su == 1) {
-                p->stage_units = su;
-                p->stages_per_slice = nst;
-                p->ring_stages = ring;
-                p->pitch = 0;
-                p->stage_bytes = stage;
-                p->x_off = box(p->R, su);
-                break;
+        auto choose = [&](int stage_weight_bytes) {
+            const int target = std::max(1, stage_weight_bytes / (p->R * hsp::kUnitBytes));
+            // the divisor of the slice nearest the target (the larger one on a tie), at
+            // most half the slice: at least two stages, so loads and products overlap
+            int su = 0;
+            for (int d = 1; d <= std::max(1, Us / 2); ++d)
+                if (Us % d == 0 && (su == 0 || std::abs(d - target) <= std::abs(su - target))) su = d;
+            for (;;) {
+                const int stage = box(p->R, su) + box(M, su);
+                const int nst = ceil_div(Us, su);
+                int ring = std::min(std::min(nst, budget / stage), kMaxRingStages);
+                if (ring >= std::min(2, nst) || su == 1) {
+                    p->stage_units = su;
+                    p->stages_per_slice = nst;
+                    p->ring_stages = ring;
+                    p->pitch = 0;
+                    p->stage_bytes = stage;
+                    p->x_off = box(p->R, su);
+                    return;
+                }
+                int d = su - 1;  // next smaller divisor of the slice
+                while (d > 1 && Us % d != 0) --d;
+                su = d;
             }
-            int d = su - 1;  // next smaller divisor of the slice
-            while (d > 1 && Us % d != 0) --d;
-            su = d;
-        }
+        };
+        choose(kStageWeightBytes);
+        // When the token rows of a stage crowd the ring down to fewer than three of
+        // several stages (M = 8 at hidden 6144 / 7168), half-size stages keep more of
+        // the slice in flight: measured on GB300, qk_indexer M = 8 8.93 -> 8.55 us,
+        // glm_fused_a M = 8 9.53 -> 9.15 us; at M = 1 the 64 KB stages stay faster.
+        // The stage width does not enter the summation order.
+        if (p->ring_stages < 3 && p->stages_per_slice > p->ring_stages) choose(kStageWeightBytes / 2);
     } else {
         const int first = Us >= 2 * p->WK ? 2 : 1;
         for (int nst = first; nst <= Us; ++nst) {
