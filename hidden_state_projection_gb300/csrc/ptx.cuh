@@ -258,8 +258,11 @@ __device__ __forceinline__ uint32_t to_tf32(uint32_t f) {
 }
 
 // Release fence at GPU scope: this thread's earlier global stores are performed
-// before anything it does afterwards (here: the dependent-launch trigger).
-__device__ __forceinline__ void fence_release_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// before anything it does afterwards (here: the dependent-launch trigger).  A
+// release-only fence: the trigger needs no acquire side (measured on GB300 a few
+// hundredths of a microsecond cheaper per call than fence.acq_rel.gpu; the ordering
+// stress test without grid-dependency waits sees no stale output with either).
+__device__ __forceinline__ void fence_release_gpu() { asm volatile("fence.release.gpu;" ::: "memory"); }
 
 // ---- programmatic dependent launch ----------------------------------------
 
