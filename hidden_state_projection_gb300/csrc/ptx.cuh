@@ -281,6 +281,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 
 // Split cluster barrier: arrive early (does not wait), wait later.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+// Arrival without release ordering: for a barrier that only keeps CTAs resident (their
+// shared memory addressable) while copies that complete on mbarriers are in flight.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Bulk copy from this CTA's shared memory into a cluster peer's shared memory

@@ -284,8 +284,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         // First half of the closing cluster barrier: my receive buffer is complete, so
         // every copy out of a peer's staging buffer into mine has landed.  The wait
         // comes last, after the trigger: no CTA leaves while a bulk copy may still read
-        // its staging buffer, yet the peers' sums, stores and fences overlap it.
-        cluster_arrive();
+        // its staging buffer, yet the peers' sums, stores and fences overlap it.  The
+        // barrier only keeps the CTAs resident (the data moved by copies that complete on
+        // mbarriers), so the arrival carries no release ordering: a release arrival here
+        // waited 0.3-1.9 us (0.7 us on average) at qk_indexer M = 64 on GB300.
+        cluster_arrive_relaxed();
         if (!aborted && got) {
             constexpr int kT4 = NT / 4;
             // consecutive threads take consecutive rows of the same four tokens
