@@ -124,8 +124,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const uint32_t tmem_d = *tmem_slot;
     if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
     // First half of a cluster barrier: the peers' receive barriers are initialised
-    // before anyone pushes into them (the wait comes after the main loop).
-    if (a.slices > 1) cluster_arrive();
+    // before anyone pushes into them (the wait comes after the main loop).  The
+    // initialising thread's fence.mbarrier_init.release.cluster, before the CTA
+    // barrier, is the release; the arrival itself is relaxed, so that the copy
+    // producer and the MMA issuer start without waiting on it.
+    if (a.slices > 1) cluster_arrive_relaxed();
 
     if (warp >= 2 && a.prefetch_l2 && nkb > 0) {
         // One contiguous run per weight row: this slice's k-blocks of that row.
