@@ -445,10 +445,13 @@ proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0,
 
 // ---- tensor-memory plan ----------------------------------------------------
 
-// bf16 with 9 <= M <= 64: the streaming kernel up to kStreamMaxM tokens, the
-// tensor-memory kernel above (measured on GB300, qk_indexer: M = 16 10.96 vs 12.13 us,
-// M = 32 17.8 vs 12.3 us); option large_m_path 1 / 2 forces one of them.
-constexpr int kStreamMaxM = 16;
+// bf16 with 9 <= M <= 64: the tensor-memory kernel.  Measured on GB300 (µs, streaming /
+// tensor memory): qk_indexer M = 9 / 12 / 16: 10.2 / 10.9, 10.7 / 10.9, 11.0 / 10.9;
+// wq_a++wkv: 8.1 / 8.8, 8.3 / 8.8, 8.5 / 8.8; glm_fused_a (2752 rows): 16.7 / 10.6,
+// 18.0 / 10.6, 18.6 / 10.6 -- its 64-row CTAs over four K slices need 172 CTAs, a second
+// wave.  The tensor-memory kernel has no such cliff, so it takes every M >= 9; option
+// large_m_path 1 / 2 forces one of them.
+constexpr int kStreamMaxM = 8;
 bool use_umma(int M, proj_dtype dt) {
     if (M <= 8 || dt != PROJ_BF16) return false;
     const int o = g_opt_large_m_path.load();

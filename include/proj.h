@@ -90,12 +90,10 @@ typedef struct {
      * to test the timeout path.  Never faults: nothing is read or written out of
      * bounds and every wait is bounded. */
     int32_t skip_stage_plus1;
-    /* Kernel for bf16 with 9 <= M <= 64: 0 (default) = the streaming mma.sync kernel
-     * (the one that also serves M <= 8, tf32 and fp32) for M <= 16 and the
-     * tensor-memory kernel (tcgen05.mma into TMEM) for M >= 17, the faster of the two
-     * measured on GB300; 1 = the streaming kernel for every M; 2 = the tensor-memory
-     * kernel for every M >= 9.  All give results within tolerance; each is bitwise
-     * self-consistent (fused = separate, run to run). */
+    /* Kernel for bf16 with 9 <= M <= 64: 0 (default) and 2 = the tensor-memory kernel
+     * (tcgen05.mma into TMEM); 1 = the streaming mma.sync kernel (the one that also
+     * serves M <= 8, tf32 and fp32).  Both give results within tolerance; each is
+     * bitwise self-consistent (fused = separate, run to run). */
     int32_t large_m_path;
     /* 1: the tensor-memory kernel first prefetches each CTA's weight rows into L2 as
      * contiguous runs.  0 (default): no prefetch (measured slower on GB300). */

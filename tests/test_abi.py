@@ -154,13 +154,13 @@ def test_pack_check_and_options(hsp):
         hsp.set_options(wait_limit_us=-1)
     with pytest.raises(hsp.ProjError):
         hsp.set_options(large_m_path=3)
-    # the default engine for bf16: streaming up to 16 tokens, tensor memory above
-    assert [hsp.describe_plan(M, 7168, 2304, 0)["engine"] for M in (1, 8, 9, 16, 17, 64)] == [0, 0, 0, 0, 1, 1]
+    # the default engine for bf16: streaming (or the register ring) up to 8 tokens, tensor memory above
+    assert [hsp.describe_plan(M, 7168, 2304, 0)["engine"] for M in (1, 8, 9, 16, 17, 64)] == [0, 0, 1, 1, 1, 1]
     hsp.set_options(large_m_path=2)
     assert [hsp.describe_plan(M, 7168, 2304, 0)["engine"] for M in (8, 9, 16, 17)] == [0, 1, 1, 1]
     # bf16 rows of at most 80 k-units (K <= 5120) at M <= 8: the register-ring kernel
     hsp.set_options(pdl=True)
-    assert [hsp.describe_plan(M, 5120, 1792, 0)["engine"] for M in (1, 4, 8, 9)] == [2, 2, 2, 0]
+    assert [hsp.describe_plan(M, 5120, 1792, 0)["engine"] for M in (1, 4, 8, 9)] == [2, 2, 2, 1]
     assert hsp.describe_plan(8, 5120, 1792, 0)["rows_per_cta"] <= 16
     assert hsp.describe_plan(8, 5112, 1792, 0)["engine"] == 0        # rows not a whole number of k-units
     assert hsp.describe_plan(1, 5120, 1792, 1)["engine"] == 3        # fp32: the register GEMV

@@ -140,8 +140,8 @@ def test_empty_batch_is_a_no_op(hsp):
 @pytest.mark.parametrize("M", [9, 16, 17, 32, 33, 64])
 @pytest.mark.parametrize("forced", [1, 2])
 def test_large_m_engines_match_oracle(hsp, M, forced):
-    """bf16 at M > 8 runs the streaming kernel up to 16 tokens and the tensor-memory
-    kernel above; either can be forced for every M, and each must agree with the oracle."""
+    """bf16 at M > 8 runs the tensor-memory kernel; the streaming kernel can be forced for
+    every M, and each must agree with the oracle."""
     K, splits = 7168, (1536, 576, 128, 64)
     x, ws = W.random_case(K, splits, M, "bf16", seed=900 + M)
     w_cat = torch.cat(ws, 0)
@@ -151,7 +151,7 @@ def test_large_m_engines_match_oracle(hsp, M, forced):
         outs = _run_both(hsp, x, w_cat, splits)
     finally:
         hsp.set_options(pdl=True, large_m_path=0)
-    assert hsp.describe_plan(M, K, sum(splits), 0)["engine"] == (1 if M > 16 else 0)
+    assert hsp.describe_plan(M, K, sum(splits), 0)["engine"] == 1
     check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"engine {forced} M{M}")
 
 
