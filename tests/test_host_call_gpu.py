@@ -102,3 +102,34 @@ def test_host_plan_argument_checks(hsp):
     assert lib.proj_host_plan_create(None, w.data_ptr(), ns, 2, oh, 1, 64, 0, x_dev.data_ptr(), od,
                                      ctypes.byref(h)) == S["PROJ_ERR_INVALID_ARG"]
     assert not h.value
+
+
+def test_host_plan_as_the_first_call_of_a_process():
+    """A plan recorded before anything else ran in the process (the library's per-device
+    set-up and first kernel configuration happen while the graph is being recorded)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = r'''
+import sys, torch
+sys.path.insert(0, %r)
+import workloads as W
+import hidden_state_projection_gb300 as hsp
+wl = W.WORKLOADS["wq_a_wkv"]
+M = 8
+w = W.weight_cat(wl).cuda()
+x_dev = torch.empty((M, wl.K), dtype=w.dtype, device="cuda")
+outs_dev = [torch.empty((M, n), dtype=w.dtype, device="cuda") for n in wl.splits]
+outs_host = [torch.zeros((M, n), dtype=w.dtype).pin_memory() for n in wl.splits]
+xh = W.activation(wl, M).pin_memory()
+plan = hsp.HostPlan(xh, w, wl.splits, outs_host, x_dev, outs_dev)
+plan(); plan()
+torch.cuda.synchronize()
+ref = hsp.fused_gemm(xh.cuda(), w, wl.splits)
+assert all(torch.equal(h, r.cpu()) for h, r in zip(outs_host, ref))
+plan.close()
+print("ok")
+''' % root
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
