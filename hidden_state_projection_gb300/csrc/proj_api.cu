@@ -258,8 +258,9 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     p->RT = p->R > p->WR * 16 ? 2 : 1;
     const int slots = p->WR * p->RT * 16;
     p->grid_x = ceil_div(n_rows, p->R);
-    // partials of the warps, plus (K slices) the receive buffer of the cluster reduction
-    const int red_bytes = p->WK * slots * 8 * p->MT * 4 + (p->S > 1 ? slots * 8 * p->MT * 4 : 0);
+    // partial sums of the warps, plus (K slices) the receive buffer of the cluster
+    // reduction; rows of 8 * MT + 1 floats (the kernel pads them against bank conflicts)
+    const int red_bytes = (p->WK * slots + (p->S > 1 ? slots : 0)) * (8 * p->MT + 1) * 4;
     const int budget = kSmemLimit - kSmemReserve;
     const int Us = p->units_per_slice;
     p->tensor = (row_bytes % hsp::kUnitBytes) == 0;

@@ -299,6 +299,10 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                       const __grid_constant__ StreamArgs a) {
     using C = StreamCfg<COMPUTE, MT, RT, WR, WK>;
     constexpr int kSlots = C::kSlots, kXRows = C::kXRows;
+    // Row pitch (floats) of the partial-sum and receive buffers: one more than the token
+    // slots, so that a warp reading one token of 32 consecutive rows hits 32 banks (with
+    // a pitch of 8 * MT the combine loop read one bank 8- to 32-fold).
+    constexpr int kXP = kXRows + 1;
 
     // The ring starts on a 1024-byte boundary (the swizzle pattern of the tensor
     // layout repeats every 1024 bytes).
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         __syncthreads();
     }
 
-    // ---- per-warp partials -> red[wk][slot][tok] (aliases the ring) ----
+    // ---- per-warp partials -> red[wk][slot][tok], row pitch kXP (aliases the ring) ----
     float *red = reinterpret_cast<float *>(smem);
     if (warp < C::kNCW && !aborted) {
         const int wk = warp % WK, wr = warp / WK;
@@ -573,7 +577,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                         v += __shfl_xor_sync(0xffffffffu, v, 4);
                         v += __shfl_xor_sync(0xffffffffu, v, 2);
                         v += __shfl_xor_sync(0xffffffffu, v, 1);
-                        if (c == 0) red[(wk * kSlots + wr * RT * 16 + g + 4 * i) * kXRows + t] = v;
+                        if (c == 0) red[(wk * kSlots + wr * RT * 16 + g + 4 * i) * kXP + t] = v;
                     }
             } else {
                 const int rl = lane & 3, tl = lane >> 2;
@@ -581,7 +585,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 for (int i = 0; i < 4 * RT; ++i)
 #pragma unroll
                     for (int j = 0; j < MT; ++j)
-                        red[(wk * kSlots + wr * RT * 16 + rl + 4 * i) * kXRows + tl + 8 * j] = acc_fo[i][j];
+                        red[(wk * kSlots + wr * RT * 16 + rl + 4 * i) * kXP + tl + 8 * j] = acc_fo[i][j];
             }
         } else {
 #pragma unroll
@@ -590,8 +594,8 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 for (int j = 0; j < MT; ++j) {
                     const int s0 = wr * RT * 16 + t * 16 + (lane >> 2);
                     const int t0 = j * 8 + 2 * (lane & 3);
-                    float *p0 = red + (wk * kSlots + s0) * kXRows + t0;
-                    float *p1 = red + (wk * kSlots + s0 + 8) * kXRows + t0;
+                    float *p0 = red + (wk * kSlots + s0) * kXP + t0;
+                    float *p1 = red + (wk * kSlots + s0 + 8) * kXP + t0;
                     float d[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -617,9 +621,9 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
             const int tok = e / kSlots, slot = e - tok * kSlots;
             if (tok >= a.M || slot >= rows_here) continue;
-            float v = red[slot * kXRows + tok];
+            float v = red[slot * kXP + tok];
 #pragma unroll
-            for (int q = 1; q < WK; ++q) v += red[(q * kSlots + slot) * kXRows + tok];
+            for (int q = 1; q < WK; ++q) v += red[(q * kSlots + slot) * kXP + tok];
             if (a.slices == 1) {
                 const int n = row0 + slot;
                 const int i = split_of(a.splits, n);
@@ -627,18 +631,18 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                     // normalized column: parked in fp32 for the split's last CTA
                     a.norm.vals[a.norm.vals_off[i] + static_cast<int64_t>(tok) * a.norm.cols[i] +
                                 (n - a.splits.off[i])] = v;
-                    red[slot * kXRows + tok] = v;
+                    red[slot * kXP + tok] = v;
                 } else {
                     store_tok<kBf16Out>(out_row<kBf16Out>(a.splits, n), tok, v);
                     stored = true;
                 }
             } else {
-                red[slot * kXRows + tok] = v;
+                red[slot * kXP + tok] = v;
             }
         }
     }
     if constexpr (NORM)
-        stored |= norm_epilogue<kBf16Out, kSlots, kXRows>(a, red, armed + a.ring_stages, row0, rows_here, aborted, tid);
+        stored |= norm_epilogue<kBf16Out, kSlots, kXP>(a, red, armed + a.ring_stages, row0, rows_here, aborted, tid);
 
     if (a.slices > 1) {
         // ---- K slices of the cluster added in slice order ----
@@ -649,7 +653,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         // sits after the partials in the ring, which every CTA has left once the
         // first barrier is passed.
         const int per = kSlots / a.slices;
-        float *recv = red + WK * kSlots * kXRows;
+        float *recv = red + WK * kSlots * kXP;
         const uint32_t recv_local = smem_u32(recv);
         // Every CTA has left its ring: its last shared-memory reads were consumed by its
         // products before the CTA barrier above, and its copies landed before it waited
@@ -663,8 +667,8 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 const int slot = e / kXRows, tok = e - slot * kXRows;
                 if (tok >= a.M || slot >= rows_here) continue;
                 const int q = slot / per;
-                const uint32_t dst = recv_local + static_cast<uint32_t>(((slice * per + slot - q * per) * kXRows + tok) * 4);
-                st_shared_cluster_f32(cluster_map_shared(dst, static_cast<uint32_t>(q)), red[slot * kXRows + tok]);
+                const uint32_t dst = recv_local + static_cast<uint32_t>(((slice * per + slot - q * per) * kXP + tok) * 4);
+                st_shared_cluster_f32(cluster_map_shared(dst, static_cast<uint32_t>(q)), red[slot * kXP + tok]);
             }
         }
         cluster_sync_all();
@@ -673,8 +677,8 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                 const int tok = e / per, rr = e - tok * per;
                 const int slot = slice * per + rr;
                 if (tok >= a.M || slot >= rows_here) continue;
-                float v = recv[rr * kXRows + tok];
-                for (int q = 1; q < a.slices; ++q) v += recv[(q * per + rr) * kXRows + tok];
+                float v = recv[rr * kXP + tok];
+                for (int q = 1; q < a.slices; ++q) v += recv[(q * per + rr) * kXP + tok];
                 store_tok<kBf16Out>(out_row<kBf16Out>(a.splits, row0 + slot), tok, v);
                 stored = true;
             }
