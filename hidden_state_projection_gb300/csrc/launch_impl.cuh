@@ -86,7 +86,7 @@ cudaError_t launch_compute(const LaunchReq &r) {
             break;
         case 2:
             if (r.MT != 8) break;
-            return rt1 ? launch_variant<COMPUTE, 8, 1, 4, 2>(r) : launch_variant<COMPUTE, 8, 2, 4, 2>(r);
+            return rt1 ? launch_variant<COMPUTE, 8, 1, 2, 4>(r) : launch_variant<COMPUTE, 8, 2, 2, 4>(r);
         default:
             break;
     }
