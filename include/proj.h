@@ -87,7 +87,8 @@ typedef struct {
     int32_t wait_limit_us;
     /* Test hook, 0 = off.  When > 0, the weight stream of every CTA leaves out
      * its stage number (value - 1), so its consumers' waits run out: used only
-     * to test the timeout path.  Never faults: nothing is read or written out of
+     * to test the timeout path (in the register-ring and register GEMV kernels,
+     * stage 0 is the token copy).  Never faults: nothing is read or written out of
      * bounds and every wait is bounded. */
     int32_t skip_stage_plus1;
     /* Kernel for bf16 with 9 <= M <= 64: 0 (default) and 2 = the tensor-memory kernel
