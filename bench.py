@@ -48,17 +48,23 @@ def dist_env():
     return ws, rank, local
 
 
-def kernel_sources_sha16():
-    import glob
+# The device-code files of each kernel family: its header, its instances and the
+# headers it includes.  A profile's DRAM counters stay valid while these are unchanged.
+KERNEL_FILES = {
+    "reg": ["reg_kernel.cuh", "kernels_reg.cu"],
+    "gemv": ["gemv_kernel.cuh", "kernels_gemv.cu"],
+    "stream": ["stream_kernel.cuh", "launch_impl.cuh", "kernels_bf16.cu", "kernels_tf32.cu", "kernels_fp32.cu"],
+    "umma": ["umma_kernel.cuh", "kernels_umma.cu"],
+}
+SHARED_FILES = ["ptx.cuh", "scatter.cuh", "norm_epilogue.cuh", "prefetch.cuh", "stream_args.h"]
+
+
+def kernel_sources_sha16(kernel: str) -> str:
     import hashlib
     csrc = os.path.join(ROOT, "hidden_state_projection_gb300", "csrc")
-    # the device code: kernel headers, the kernel translation units and the argument
-    # structs (host-only files such as the C ABI do not change what a kernel does)
-    files = sorted(glob.glob(os.path.join(csrc, "kernels_*.cu"))) + sorted(glob.glob(os.path.join(csrc, "*.cuh"))) \
-        + [os.path.join(csrc, "stream_args.h")]
     h = hashlib.sha256()
-    for f in files:
-        with open(f, "rb") as fh:
+    for f in KERNEL_FILES[kernel] + SHARED_FILES:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -71,13 +77,16 @@ def profiled_traffic(name, M):
     if not paths:
         return None
     path = paths[0]
+    kernel = os.path.basename(path).split("_")[1]          # hsp_<kernel>_kernel_<workload>_m<M>.md
+    if kernel not in KERNEL_FILES:
+        return None
     fields = {}
     with open(path) as f:
         for line in f:
             if ":" in line and not line.startswith(("#", "|", " ")):
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-    if fields.get("kernel_sources_sha256_16") != kernel_sources_sha16():
+    if fields.get("kernel_sources_sha256_16") != kernel_sources_sha16(kernel):
         return None
     try:
         return int(fields["traffic_bytes_per_launch"])
