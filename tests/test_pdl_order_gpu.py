@@ -62,8 +62,9 @@ def _stress(hsp, consumer, name, M, separate, wait, early, replays=REPLAYS):
     x = W.activation(wl, M).cuda()
     w = W.weight_cat(wl).cuda()
     total = M * wl.n_total
-    assert total % 2 == 0
-    flat = torch.empty(total, dtype=torch.bfloat16, device="cuda")
+    dt = x.dtype                             # bf16, or fp32 for the indexer / router
+    assert (total * x.element_size()) % 4 == 0
+    flat = torch.empty(total, dtype=dt, device="cuda")
     views, off = [], 0
     for n in wl.splits:                      # dense [M, N_i] outputs inside one buffer
         views.append(flat[off:off + M * n].view(M, n))
@@ -71,7 +72,7 @@ def _stress(hsp, consumer, name, M, separate, wait, early, replays=REPLAYS):
     fn = hsp.separate_gemm if separate else hsp.fused_gemm
     ref = torch.cat([o.reshape(-1) for o in hsp.fused_gemm(x, w, wl.splits)])
     counter = torch.zeros(1, dtype=torch.int64, device="cuda")
-    n_words = total // 2
+    n_words = total * x.element_size() // 4
     hsp.set_options(pdl=True, trigger_early=early)
     try:
         s = torch.cuda.Stream()
@@ -84,7 +85,7 @@ def _stress(hsp, consumer, name, M, separate, wait, early, replays=REPLAYS):
         with torch.cuda.graph(g):
             stream = torch.cuda.current_stream().cuda_stream
             for _ in range(PER_GRAPH):
-                flat.view(torch.int16).fill_(-1)          # 0xFFFF: a bf16 NaN
+                flat.view(torch.int32).fill_(-1)          # all ones: NaN in bf16 and fp32
                 fn(x, w, wl.splits, outs=views)
                 rc = consumer.pdl_consumer_launch(flat.data_ptr(), ref.data_ptr(), n_words, int(wait),
                                                   counter.data_ptr(), stream)
@@ -100,7 +101,10 @@ def _stress(hsp, consumer, name, M, separate, wait, early, replays=REPLAYS):
     return int(counter.item())
 
 
-CASES = [("wq_a_wkv_m1", 1, False), ("wq_a_wkv", 8, False), ("wq_a_wkv", 4, True), ("qk_indexer", 64, False)]
+# one case per engine: the register ring (wq_a++wkv), the streaming ring (qk_indexer M = 8),
+# the tensor-memory kernel (qk_indexer M = 64), the fp32 register GEMV (indexer fp32 M = 4)
+CASES = [("wq_a_wkv_m1", 1, False), ("wq_a_wkv", 8, False), ("wq_a_wkv", 4, True), ("qk_indexer", 8, False),
+         ("qk_indexer", 64, False), ("indexer_fp32", 4, False)]
 
 
 @pytest.mark.parametrize("name,M,separate", CASES)
