@@ -1,4 +1,4 @@
-// gemv_kernel.cuh -- the fp32 register GEMV kernel (PROJ_FP32, 1 <= M <= 8).
+// gemv_kernel.cuh -- the fp32 register GEMV kernel (PROJ_FP32, 1 <= M <= 64).
 //
 // Same operation and split epilogue as the other kernels (TensorRT-LLM PR #20636,
 // Description), for the fp32 projections the pages run at decode size: the indexer's
@@ -23,6 +23,12 @@
 //     bits; the chains are at most 16 terms long, well inside the fp32 tolerance;
 //   * every storing thread fences, the CTA synchronises, and only then is the dependent
 //     launch triggered (the trigger follows the stores).
+//
+// More tokens than shared memory holds (M * K * 4 > 192 KB, or M > 8) are cut into
+// grid.y groups of ceil(M / grid.y) tokens (the last one ragged); the CTAs of one row
+// slab and different groups read the same weight rows, the first from HBM and the others
+// mostly from L2, so those loads keep the normal L2 priority.  A token's sums do not
+// depend on its group: every output is one CTA's fixed-order sum over all of K.
 //
 // The one barrier wait (the token copy) is bounded; on expiry the kernel records
 // PROJ_ERR_TIMEOUT, skips its stores, waits (bounded) for its copy and returns.
@@ -51,6 +57,13 @@ __device__ __forceinline__ uint4 ldg_stream16(const char *p, uint64_t policy) {
     return v;
 }
 
+// L2 policy for weights that other CTAs (the other token groups) read again soon.
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -59,18 +72,28 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
 }
 
 __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_constant__ StreamArgs a) {
-    extern __shared__ __align__(16) float xs[];     // [M][K]
+    extern __shared__ __align__(16) float xs[];     // [tokens of the group][K]
     __shared__ float part[kGemvWarps][kGemvRows][8];  // warp sums of a block [warp][row][token]
     __shared__ __align__(8) uint64_t xfull;
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // token group: grid.y groups of ceil(M / grid.y) tokens, the last one ragged
+    const int group = static_cast<int>((a.M + gridDim.y - 1) / gridDim.y);
+    const int tok0 = static_cast<int>(blockIdx.y) * group;
+    const int Mh = min(group, a.M - tok0);
+    if (Mh < 1) {  // an empty group (the planner never makes one): nothing to do
+        griddep_launch_dependents();
+        return;
+    }
     const int row0 = blockIdx.x * a.rows_per_cta;
     const int rows_here = min(a.rows_per_cta, a.n_rows - row0);
     const int nblk = (rows_here + kGemvRows - 1) / kGemvRows;
     const int chunks = static_cast<int>(a.row_bytes >> 4);
     const int K = chunks * 4;
-    const uint64_t policy = l2_policy_evict_first();
+    // with one group every weight is read once; with several the other groups' CTAs read
+    // the same rows at about the same time, from L2
+    const uint64_t policy = gridDim.y > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
 
     uint4 buf0[kGemvRows][kGemvSteps], buf1[kGemvRows][kGemvSteps];
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -101,9 +124,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_
     griddep_wait();
     const bool x_issued = a.skip_stage != 0;  // test hook: stage 0 of this kernel is its token copy
     if (tid == 0 && x_issued) {
-        const uint32_t bytes = static_cast<uint32_t>(a.M) * static_cast<uint32_t>(a.row_bytes);
+        const uint32_t bytes = static_cast<uint32_t>(Mh) * static_cast<uint32_t>(a.row_bytes);
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_g2s(smem_u32(xs), a.x, bytes, bar);
+        bulk_copy_g2s(smem_u32(xs), a.x + static_cast<int64_t>(tok0) * a.row_bytes, bytes, bar);
     }
     if (warp == kGemvWarps - 1 && a.prefetch.count > 0)
         prefetch_ranges_l2(a.prefetch, blockIdx.x, gridDim.x, lane);
@@ -146,7 +169,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_
                 if (c < chunks) {
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
-                        if (t < a.M) {
+                        if (t < Mh) {
                             const float4 xv = *reinterpret_cast<const float4 *>(xs + t * K + c * 4);
 #pragma unroll
                             for (int r = 0; r < kGemvRows; ++r) {
@@ -169,7 +192,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_
         for (int r = 0; r < kGemvRows; ++r)
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                if (t < a.M) {
+                if (t < Mh) {
                     float v = acc[r][t];
                     v += __shfl_xor_sync(0xffffffffu, v, 16);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);
@@ -180,8 +203,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_
                 }
             }
         __syncthreads();
-        if (abort_flag == 0 && tid < kGemvRows * a.M) {
-            const int r = tid / a.M, t = tid - r * a.M;
+        if (abort_flag == 0 && tid < kGemvRows * Mh) {
+            const int r = tid / Mh, t = tid - r * Mh;
             const int row = b * kGemvRows + r;
             if (row < rows_here) {
                 float v = part[0][r][t];
@@ -190,7 +213,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_
                 const int n = row0 + row;
                 const int i = split_of(a.splits, n);
                 float *o = static_cast<float *>(a.splits.out[i]);
-                o[static_cast<int64_t>(t) * a.splits.rows[i] + (n - a.splits.off[i])] = v;
+                o[static_cast<int64_t>(tok0 + t) * a.splits.rows[i] + (n - a.splits.off[i])] = v;
                 stored = true;
             }
         }

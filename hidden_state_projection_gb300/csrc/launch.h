@@ -57,8 +57,8 @@ constexpr int kRegDepthHost = 5;
 
 // fp32 register GEMV launch (PROJ_FP32, M <= 8, K <= 8192, M * K * 4 <= kGemvMaxTokenBytes).
 struct GemvLaunchReq {
-    dim3 grid;       // (row CTAs, 1, 1)
-    int smem_bytes;  // the tokens: M * K * 4
+    dim3 grid;       // (row CTAs, token groups, 1)
+    int smem_bytes;  // the tokens of one group: ceil(M / groups) * K * 4
     int pdl;
     cudaStream_t stream;
     StreamArgs args;  // w, x, row_bytes, n_rows, rows_per_cta, M, hooks, splits, prefetch

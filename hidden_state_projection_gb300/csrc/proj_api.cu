@@ -655,32 +655,49 @@ proj_status launch_reg_rows(const DeviceInfo &dev, const void *x, const void *w,
     return PROJ_OK;
 }
 
-// ---- fp32 register GEMV plan (PROJ_FP32, M <= 8) ------------------------------
+// ---- fp32 register GEMV plan (PROJ_FP32) ---------------------------------------
 
-// PROJ_FP32 with M <= 8, K <= 8192 and the tokens within 192 KB of shared memory runs
-// the register GEMV kernel: one CTA per ceil(N / SMs) rows and all of K, no clusters
-// (measured on GB300: indexer wk ++ weights_proj 192 x 7168 and the GLM router 256 x 6144;
-// numbers in the design notes).  Option reg_path 1 turns it off.  The choice depends on
-// (M, K, dtype) only.
+// Tokens one GEMV CTA holds in shared memory: at most 8, within 192 KB.
+int gemv_group_cap(int K) {
+    const int64_t cap = hsp::kGemvMaxTokenBytes / (static_cast<int64_t>(K) * 4);
+    return static_cast<int>(std::min<int64_t>(8, cap));
+}
+
+// PROJ_FP32 with K <= 8192 and at most gemv_group_cap(K) tokens runs the register GEMV
+// kernel: one CTA per slab of rows and all of K, no clusters (measured on GB300: indexer
+// wk ++ weights_proj 192 x 7168 and the GLM router 256 x 6144; numbers in the design
+// notes).  Option reg_path 2 also sends more tokens (up to 64) to it, cut into token
+// groups along grid.y: every group's CTAs read all of their tokens and their rows'
+// weights again, and on GB300 that lost to the streaming kernel's K slices at every
+// M > 8 but one (so it is not the default).  Option reg_path 1 turns the kernel off.
+// The choice depends on (M, K, dtype) only.
 bool use_gemv(int M, int K, proj_dtype dt) {
-    if (dt != PROJ_FP32 || M < 1 || M > 8 || K > 8192) return false;
-    if (g_opt_reg_path.load() == 1) return false;
-    return static_cast<int64_t>(M) * K * 4 <= hsp::kGemvMaxTokenBytes;
+    if (dt != PROJ_FP32 || M < 1 || M > 64 || K > 8192) return false;
+    const int path = g_opt_reg_path.load();
+    if (path == 1) return false;
+    const int cap = gemv_group_cap(K);
+    return cap >= 1 && (M <= cap || path == 2);
 }
 
 struct GemvPlan {
-    int R, grid, smem;
+    int R, grid, groups, group_tokens, smem;
 };
 
+// Token groups: G = ceil(M / cap), each of ceil(M / G) tokens (so no group is empty);
+// row slabs: as many as fit beside G groups in one wave of one CTA per SM.
 void make_gemv_plan(int M, int K, int n_rows, int sms, GemvPlan *p) {
-    p->R = std::max(1, ceil_div(n_rows, std::max(1, sms)));
+    const int cap = std::max(1, gemv_group_cap(K));
+    p->groups = ceil_div(M, cap);
+    p->group_tokens = ceil_div(M, p->groups);
+    const int slabs = std::max(1, std::max(1, sms) / p->groups);
+    p->R = std::max(1, ceil_div(n_rows, slabs));
     p->grid = ceil_div(n_rows, p->R);
-    p->smem = M * K * 4;
+    p->smem = p->group_tokens * K * 4;
 }
 
 void gemv_plan_info(int M, int K, const GemvPlan &p, proj_plan_info *i) {
     memset(i, 0, sizeof *i);
-    i->bucket = 0;
+    i->bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
     i->compute = hsp::kFmaFp32;
     i->rows_per_cta = p.R;
     i->row_ctas = p.grid;
@@ -688,7 +705,7 @@ void gemv_plan_info(int M, int K, const GemvPlan &p, proj_plan_info *i) {
     i->k_warps = 16;
     i->row_warps = 1;
     i->row_tiles = 1;
-    i->token_tiles = 1;
+    i->token_tiles = p.groups;  // token groups (grid.y)
     i->ring_stages = 2;  // row blocks in flight
     i->stage_bytes = 0;
     i->smem_bytes = p.smem;
@@ -706,7 +723,7 @@ proj_status launch_gemv_rows(const DeviceInfo &dev, const void *x, const void *w
     GemvPlan p;
     make_gemv_plan(M, K, n_rows, dev.sms, &p);
     hsp::GemvLaunchReq r{};
-    r.grid = dim3(static_cast<unsigned>(p.grid), 1, 1);
+    r.grid = dim3(static_cast<unsigned>(p.grid), static_cast<unsigned>(p.groups), 1);
     r.smem_bytes = p.smem;
     r.pdl = g_opt_pdl.load();
     r.stream = stream;

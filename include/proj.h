@@ -107,12 +107,15 @@ typedef struct {
     /* bf16 with M <= 2: 0 (default) = mma.sync like 3 <= M <= 8; 1 = fp32 FMA on the
      * CUDA cores.  Both within tolerance, each bitwise self-consistent. */
     int32_t small_m_path;
-    /* Register kernels for M <= 8.  bf16 with K a multiple of 64: 0 (default) = the
+    /* Register kernels.  bf16, M <= 8 and K a multiple of 64: 0 (default) = the
      * register-ring kernel (sixteen warps load the weights straight into registers, the
      * tokens arrive as one tensor copy) when a row has at most 80 k-units of 128 bytes
      * (K <= 5120), the streaming kernel otherwise; 2 = the register-ring kernel up to 128
-     * k-units (K <= 8192).  PROJ_FP32 with K <= 8192 and M * K * 4 <= 192 KB: 0 and 2 =
-     * the register GEMV kernel (one CTA per ceil(N / SMs) rows, all of K, no K slices).
+     * k-units (K <= 8192).  PROJ_FP32 with K <= 8192: 0 = the register GEMV kernel (a CTA
+     * owns a slab of rows and all of K, no K slices) when the M tokens fit one CTA (at
+     * most 8 and M * K * 4 <= 192 KB), the streaming kernel otherwise; 2 = the register
+     * GEMV kernel up to M = 64, the tokens in groups that fit, one group per CTA along
+     * grid.y (slower than the streaming kernel on GB300 at most such M).
      * 1 = the streaming kernel for both.  All within tolerance, each bitwise
      * self-consistent (fused = separate, run to run, graph = eager). */
     int32_t reg_path;
@@ -139,8 +142,9 @@ typedef struct {
     int32_t engine;          /* 0 streaming mma.sync / FMA kernel, 1 tensor-memory (tcgen05) kernel,
                               * 2 register-ring kernel (bf16, M <= 8: ring_stages = k-units in flight per
                               * warp, stages_total = k-units per warp, stage_bytes = 0),
-                              * 3 fp32 register GEMV (M <= 8: ring_stages = row blocks in flight,
-                              * stages_total = row blocks of two rows, stage_bytes = 0) */
+                              * 3 fp32 register GEMV (M <= 64: ring_stages = row blocks in flight,
+                              * stages_total = row blocks of two rows, token_tiles = token groups
+                              * along grid.y, stage_bytes = 0) */
     int32_t tensor_copies;   /* streaming kernel: 1 = one 3-D tensor copy per stage for the weights
                               * and one for the tokens (rows a multiple of 128 bytes), 0 = one 1-D
                               * bulk copy per row and stage (any other K); register-ring kernel: 1

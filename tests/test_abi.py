@@ -114,9 +114,14 @@ def test_plan_fits_the_hardware(hsp):
                     assert p["smem_bytes"] <= 232448
                     assert p["row_ctas"] * p["rows_per_cta"] >= n
                     assert p["slices"] in (1, 2, 4, 8, 16)
-                    if p["engine"] == 3:     # fp32 register GEMV: M <= 8, all of K per CTA
-                        assert M <= 8 and dt == 1 and p["slices"] == 1 and p["threads"] == 512
-                        assert p["smem_bytes"] == M * wl.K * 4 <= 192 * 1024
+                    if p["engine"] == 3:     # fp32 register GEMV: all of K per CTA, one token group
+                        assert dt == 1 and p["slices"] == 1 and p["threads"] == 512
+                        cap = min(8, 192 * 1024 // (wl.K * 4))
+                        groups = -(-M // cap)
+                        assert p["token_tiles"] == groups
+                        assert p["smem_bytes"] == -(-M // groups) * wl.K * 4 <= 192 * 1024
+                        assert (groups - 1) * -(-M // groups) < M          # no empty group
+                        assert p["row_ctas"] * groups <= 152
                     elif p["engine"] == 2:   # register-ring kernel: bf16, M <= 8, 16 warps split K
                         assert M <= 8 and dt == 0 and wl.K * 2 % 128 == 0
                         assert p["rows_per_cta"] <= 16 and p["threads"] == 512 and p["slices"] == 1
@@ -172,6 +177,13 @@ def test_pack_check_and_options(hsp):
     # fp32 at M <= 8 with the tokens within 192 KB: the register GEMV; tf32 keeps the tensor cores
     hsp.set_options(pdl=True)
     assert [hsp.describe_plan(M, 7168, 192, 1)["engine"] for M in (1, 4, 6, 7, 9)] == [3, 3, 3, 0, 0]
+    assert [hsp.describe_plan(M, 6144, 256, 1)["engine"] for M in (8, 9)] == [3, 0]
+    # forced: more tokens than one CTA holds (6 rows of 7168 floats within 192 KB) go in groups
+    hsp.set_options(reg_path=2)
+    assert [hsp.describe_plan(M, 7168, 192, 1)["engine"] for M in (1, 7, 16, 64)] == [3] * 4
+    assert [hsp.describe_plan(M, 7168, 192, 1)["token_tiles"] for M in (6, 7, 16, 64)] == [1, 2, 3, 11]
+    assert hsp.describe_plan(64, 7168, 192, 1)["smem_bytes"] == 6 * 7168 * 4
+    hsp.set_options(reg_path=0)
     assert [hsp.describe_plan(M, 6144, 256, 1)["engine"] for M in (1, 8)] == [3, 3]
     assert hsp.describe_plan(1, 7168, 192, 2)["engine"] == 0
     assert hsp.describe_plan(1, 8196, 192, 1)["engine"] == 0            # K past 8192

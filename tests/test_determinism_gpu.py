@@ -91,7 +91,8 @@ def test_launch_counting(hsp):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("name,M", [("wq_a_wkv_m1", 1), ("qk_indexer", 8), ("qk_indexer", 64), ("indexer_fp32", 1)])
+@pytest.mark.parametrize("name,M", [("wq_a_wkv_m1", 1), ("qk_indexer", 8), ("qk_indexer", 64), ("indexer_fp32", 1),
+                                    ("indexer_fp32", 64)])
 def test_bounded_wait_reports_timeout(hsp, name, M):
     import hidden_state_projection_gb300 as m
     wl, x, w = _inputs(name, M, 0)

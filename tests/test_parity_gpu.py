@@ -190,19 +190,25 @@ def test_register_ring_and_streaming_engines_match_oracle(hsp, K, splits, reg_pa
 
 
 @pytest.mark.parametrize("K,splits", [(7168, (128, 64)), (6144, (256,)), (1536, (200, 56)), (4096, (5000,))])
-@pytest.mark.parametrize("reg_path", [0, 1])
+@pytest.mark.parametrize("reg_path", [0, 1, 2])
 def test_fp32_register_gemv_and_streaming_match_oracle(hsp, K, splits, reg_path):
-    """fp32 at M <= 8: the register GEMV kernel (default; rows in blocks of two, all of K
-    per CTA, 5000 rows = 33 rows per CTA exercises the block loop) and the streaming
-    kernel (reg_path 1) both meet the fp32 tolerance, fused and separate."""
+    """fp32: the register GEMV kernel (default while the tokens fit one CTA; rows in
+    blocks of two, all of K per CTA, 5000 rows = 33 or more rows per CTA exercises the
+    block loop; forced with reg_path 2, tokens past what one CTA holds go in groups
+    along grid.y, the last one ragged: M = 7 at K = 7168 is 4 + 3, M = 17 is 6 + 6 + 5,
+    M = 40 at K = 6144 is 8 x 5) and the streaming kernel (reg_path 1) all meet the
+    fp32 tolerance, fused and separate."""
     hsp.set_options(pdl=True, reg_path=reg_path)
     try:
-        for M in (1, 3, 4, 8):
-            if M * K * 4 > 192 * 1024 and reg_path == 0:
-                continue
+        for M in (1, 3, 4, 7, 8, 17, 40, 64):
             x, ws = W.random_case(K, splits, M, "fp32", seed=1700 + M + K)
             w_cat = torch.cat(ws, 0)
-            assert hsp.describe_plan(M, K, sum(splits), 1)["engine"] == (3 if reg_path == 0 else 0)
+            plan = hsp.describe_plan(M, K, sum(splits), 1)
+            cap = min(8, 192 * 1024 // (K * 4))
+            gemv = reg_path == 2 or (reg_path == 0 and M <= cap)
+            assert plan["engine"] == (3 if gemv else 0)
+            if gemv:
+                assert plan["token_tiles"] == -(-M // cap)
             outs = _run_both(hsp, x, w_cat, splits)
             check_close(outs, oracle_outputs(x, w_cat, splits), "fp32", f"reg_path {reg_path} K{K} M{M}")
     finally:

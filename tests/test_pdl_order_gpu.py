@@ -102,9 +102,10 @@ def _stress(hsp, consumer, name, M, separate, wait, early, replays=REPLAYS):
 
 
 # one case per engine: the register ring (wq_a++wkv), the streaming ring (qk_indexer M = 8),
-# the tensor-memory kernel (qk_indexer M = 64), the fp32 register GEMV (indexer fp32 M = 4)
+# the tensor-memory kernel (qk_indexer M = 64), the fp32 register GEMV (indexer fp32 M = 4),
+# the streaming kernel's fp32 FMA path (indexer fp32 M = 64)
 CASES = [("wq_a_wkv_m1", 1, False), ("wq_a_wkv", 8, False), ("wq_a_wkv", 4, True), ("qk_indexer", 8, False),
-         ("qk_indexer", 64, False), ("indexer_fp32", 4, False)]
+         ("qk_indexer", 64, False), ("indexer_fp32", 4, False), ("indexer_fp32", 64, False)]
 
 
 @pytest.mark.parametrize("name,M,separate", CASES)
