@@ -59,13 +59,23 @@ KERNEL_FILES = {
 SHARED_FILES = ["ptx.cuh", "scatter.cuh", "norm_epilogue.cuh", "prefetch.cuh", "stream_args.h"]
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without // and /* */ comments and blank lines (string literals kept)."""
+    import re
+    tok = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
+    code = tok.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", src)
+    return "\n".join(ln.rstrip() for ln in code.splitlines() if ln.strip())
+
+
 def kernel_sources_sha16(kernel: str) -> str:
+    """Hash of a kernel's device sources (its header, its instances and the headers they
+    include), comments left out: a comment edit does not void a profile."""
     import hashlib
     csrc = os.path.join(ROOT, "hidden_state_projection_gb300", "csrc")
     h = hashlib.sha256()
     for f in KERNEL_FILES[kernel] + SHARED_FILES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -260,9 +270,10 @@ def time_graph(g, steps, warmup, barrier=None):
 def time_e2e(hsp, st: Setup, calls: int):
     """Public API with host buffers: every step copies its tokens from pinned host memory
     to the device, runs the fused projection and returns the outputs to pinned host memory
-    (proj_fused_gemm_host through a bound HostCall: one foreign call per step; the kernel
-    stores the outputs straight into the mapped host buffers), cycling the weight copies
-    as the kernel-only timing does.  Also timed: the same steps as recorded host plans
+    (proj_fused_gemm_host through a bound HostCall: one foreign call per step; a staging
+    kernel reads the tokens from the mapped host buffer and the projection kernel stores
+    the outputs straight into the mapped host buffers), cycling the weight copies as the
+    kernel-only timing does.  Also timed: the same steps as recorded host plans
     (proj_host_plan_launch, one graph launch per step)."""
     dev = st.x[0].device
     xh = [st.x[c].cpu().pin_memory() for c in range(4)]
@@ -392,7 +403,7 @@ def run_ours(args):
                      "bytes_per_call": bytes_call, "us_per_call_per_gpu": round(ms_per_step * 1000.0 / args.calls, 4)},
         "e2e": {"value": round(e2e_us, 3), "unit": "µs/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "public API proj_fused_gemm_host per step (bound HostCall): H2D copy of x from pinned memory, fused call, outputs stored by the kernel into pinned mapped host memory",
+                "how": "public API proj_fused_gemm_host per step (bound HostCall): x read from pinned host memory by the token staging kernel, fused call (PDL-chained), outputs stored by the kernel into pinned mapped host memory",
                 "host_plan_us": round(e2e_plan_us, 3)},
         "gpu_launches": args.steps * args.calls,   # one fused kernel per call, all inside the graph
         "with_l2_prefetch_of_next_weights": {

@@ -223,8 +223,9 @@ class HostCall:
     step): proj_fused_gemm_host with its ctypes arguments built here, so each call is one
     foreign-function call.  x_host / outs_host are pinned CPU tensors, x_dev / outs_dev
     device staging tensors of the same shapes; w_cat stays on the device.  Calling the
-    object enqueues H2D copy, projection and D2H copies on the stream; synchronise before
-    reading outs_host."""
+    object enqueues the token copy (a staging kernel when x_host is pinned, else a
+    copy-engine copy), the projection and, for outputs not in pinned memory, D2H copies on
+    the stream; synchronise before reading outs_host."""
 
     def __init__(self, x_host: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
                  outs_host: Sequence[torch.Tensor], x_dev: torch.Tensor, outs_dev: Sequence[torch.Tensor],

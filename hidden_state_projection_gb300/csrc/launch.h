@@ -55,7 +55,7 @@ cudaError_t launch_reg(const RegLaunchReq &r);
 constexpr int kRegThreadsHost = 16 * 32;
 constexpr int kRegDepthHost = 5;
 
-// fp32 register GEMV launch (PROJ_FP32, M <= 8, K <= 8192, M * K * 4 <= kGemvMaxTokenBytes).
+// fp32 register GEMV launch (PROJ_FP32, K <= 8192; one token group per CTA along grid.y).
 struct GemvLaunchReq {
     dim3 grid;       // (row CTAs, token groups, 1)
     int smem_bytes;  // the tokens of one group: ceil(M / groups) * K * 4
@@ -66,6 +66,10 @@ struct GemvLaunchReq {
 cudaError_t launch_gemv(const GemvLaunchReq &r);
 constexpr int kGemvThreadsHost = 16 * 32;
 constexpr int kGemvMaxTokenBytes = 192 * 1024;
+
+// Token staging for the host entry point: n16 16-byte chunks from `src` (the device
+// address of page-locked host memory) to `dst`, at most max_ctas CTAs, PDL-chained.
+cudaError_t launch_stage(const void *src, void *dst, int64_t n16, int max_ctas, int pdl, cudaStream_t stream);
 
 // Threads per CTA of a bucket (eight consumer warps + one producer warp).
 constexpr int kThreadsPerCta = 9 * 32;

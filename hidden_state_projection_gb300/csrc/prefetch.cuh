@@ -1,9 +1,9 @@
 // prefetch.cuh -- L2 prefetch of caller-named tensors (weights of later kernels).
 //
 // TensorRT-LLM PR #20502 (GLM-5.2 decode target), glmFusedAGemm commit message:
-// before the grid-dependency wait each CTA prefetches up to four caller tensors --
-// weights that later kernels of the step read -- into L2 in 16 KB bulk prefetches
-// spread over the CTAs.  Here chunk c of the concatenated ranges goes to CTA
+// ahead of its grid-dependency wait, the GLM fused-A kernel has its CTAs share out
+// 16 KB L2 bulk prefetches of as many as four caller tensors (the weights the step's
+// following kernels will need).  Here chunk c of the concatenated ranges goes to CTA
 // (c mod CTAs), lane-parallel inside the calling warp.  The streaming kernel issues
 // them after its own weight and token copies (measured: ahead of the token copies
 // they delay the first stage), the tensor-memory kernel before its grid wait.

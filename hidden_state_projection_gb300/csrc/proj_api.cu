@@ -1058,8 +1058,33 @@ proj_status proj_fused_gemm_host(const void *x_host, const void *w_cat, const in
         if (!outs_host[i]) return fail(PROJ_ERR_INVALID_ARG, "outs_host[%d] is NULL", i);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const size_t esz = static_cast<size_t>(elem_size(dtype));
-    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, static_cast<size_t>(M) * K * esz, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (tokens to the device)");
+    const size_t x_bytes = static_cast<size_t>(M) * K * esz;  // a multiple of 16 (validated row size)
+    // Tokens in page-locked host memory that the device can address are copied by the
+    // staging kernel, chained to the projection by programmatic dependent launch; any
+    // other host buffer (pageable memory) goes through a copy-engine copy.
+    const void *x_src = nullptr;
+    {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, x_host) == cudaSuccess) {
+            if (pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+                (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15u) == 0 &&
+                (reinterpret_cast<uintptr_t>(x_dev) & 15u) == 0)
+                x_src = pa.devicePointer;
+        } else {
+            (void)cudaGetLastError();  // pageable memory: not an error, copy it
+        }
+    }
+    cudaError_t e;
+    if (x_src) {
+        DeviceInfo dev;
+        if ((st = device_info(&dev)) != PROJ_OK) return st;
+        e = hsp::launch_stage(x_src, x_dev, static_cast<int64_t>(x_bytes / 16), dev.sms, g_opt_pdl.load(), s);
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch (token staging)");
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    } else {
+        e = cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (tokens to the device)");
+    }
     // An output in page-locked host memory that the device can address (mapped, as
     // cudaHostAlloc memory is under unified addressing) is written by the kernel itself,
     // over the host link, instead of through a staging buffer and a copy; the stream's

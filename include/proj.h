@@ -153,9 +153,9 @@ typedef struct {
 } proj_plan_info;
 
 /*
- * proj_fused_gemm -- the fused projection (TensorRT-LLM PR #20636, Description:
- * "both projections run as a single tinygemm2 over the concatenated weight"; here
- * for any M in 1..PROJ_MAX_M).  One kernel launch streams every row of w_cat
+ * proj_fused_gemm -- the fused projection (TensorRT-LLM PR #20636, Description: the
+ * two projections become one GEMM over the row-concatenated weight; here for any M in
+ * 1..PROJ_MAX_M).  One kernel launch streams every row of w_cat
  * once and writes outs[i][m * n_splits[i] + r] = round(sum_k x[m,k] * w_cat[off_i + r, k]).
  *   x          device [M, K]
  *   w_cat      device [N_total, K], N_total = sum(n_splits)
@@ -174,10 +174,10 @@ proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_s
 /*
  * proj_fused_gemm_prefetch -- proj_fused_gemm that also prefetches up to
  * PROJ_MAX_PREFETCH caller-named global ranges into L2 (TensorRT-LLM PR #20502,
- * glmFusedAGemm commit message: before the grid-dependency wait each CTA prefetches
- * up to four caller tensors -- weights that later kernels of the step read -- into
- * L2 in 16 KB bulk prefetches spread over the CTAs; here the streaming kernel
- * issues them right after its own copies).  The ranges are only read as a hint:
+ * glmFusedAGemm commit message: ahead of its grid-dependency wait, the GLM fused-A
+ * kernel has its CTAs share out 16 KB L2 bulk prefetches of as many as four caller
+ * tensors, the weights the step's following kernels will need; here the streaming
+ * kernel issues them right after its own copies).  The ranges are only read as a hint:
  * the outputs are bitwise those of proj_fused_gemm.  Ranges must stay allocated
  * until the call has completed on the stream.
  */
@@ -190,7 +190,8 @@ proj_status proj_fused_gemm_prefetch(const void *x, const void *w_cat, const int
  * proj_fused_gemm_rmsnorm -- proj_fused_gemm followed, in the same kernel, by the
  * RMSNorm its consumers apply (TensorRT-LLM PR #20636, Description: the q_norm /
  * kv_norm RMSNorms read the wq_a / wkv outputs; PR #20502, glm_mla_kv_half_append
- * commit message: RMSNorm of the 512 latent columns of the raw kv_a_proj output).
+ * commit message: the kv_a_proj output's 512 latent columns, not its RoPE part, are
+ * normalised).
  * For split i with c = norm_cols[i] > 0, every token m and r < c:
  *     outs[i][m, r] = round(y[m, r] / sqrt(mean_{j < c} y[m, j]^2 + eps) * gammas[i][r])
  * with y the fp32 sums of the projection (one rounding per output); columns r >= c,
@@ -249,13 +250,17 @@ proj_status proj_fused_gemm_rmsnorm_static(const void *x, const void *w_cat, con
 /*
  * proj_fused_gemm_host -- proj_fused_gemm for a caller whose tokens and results live in
  * host memory (a decode step that receives the hidden state from the host and hands the
- * projections back to it).  Enqueued on `stream`, in this order: one host-to-device copy
- * of x_host into x_dev (M * K elements), the fused projection from x_dev into outs_dev
- * (exactly proj_fused_gemm: same kernel, same bits), one device-to-host copy of each
- * outs_dev[i] into outs_host[i].  An outs_host[i] in page-locked memory that the device
- * can address (cudaHostAlloc memory under unified addressing) is instead written by the
- * kernel directly, over the host link, and outs_dev[i] is left untouched.  The call
- * returns once everything is enqueued; synchronise the stream before reading outs_host.
+ * projections back to it).  Enqueued on `stream`, in this order: x_host copied into
+ * x_dev (M * K elements), the fused projection from x_dev into outs_dev (exactly
+ * proj_fused_gemm: same kernel, same bits), one device-to-host copy of each outs_dev[i]
+ * into outs_host[i].  When x_host is page-locked memory that the device can address
+ * (cudaHostAlloc memory under unified addressing), the token copy is a small staging
+ * kernel that reads it over the host link, launched with programmatic dependent launch
+ * like the projection (2 kernel launches per call); otherwise it is one host-to-device
+ * cudaMemcpyAsync.  An outs_host[i] in such memory is likewise written by the kernel
+ * directly, and outs_dev[i] is left untouched.  The call returns once everything is
+ * enqueued; synchronise the stream before reading outs_host, and do not change x_host
+ * before the stream has passed the call.
  *   x_host     host [M, K]; page-locked (cudaHostAlloc / pinned) for the copies to be
  *              asynchronous, pageable memory makes the copy synchronous
  *   outs_host  host array of num_splits host pointers, outs_host[i] is [M, N_i]
@@ -271,7 +276,7 @@ proj_status proj_fused_gemm_host(const void *x_host, const void *w_cat, const in
 
 /*
  * Host plans -- proj_fused_gemm_host bound once to fixed buffers and recorded as one CUDA
- * graph (the host-to-device copy, the fused projection, the device-to-host copies), so
+ * graph (the token copy, the fused projection, the device-to-host copies), so
  * that a loop repeating the step (decode) costs one graph launch per step on the host.
  * proj_host_plan_create takes the arguments of proj_fused_gemm_host (x_host and every
  * outs_host[i] must be page-locked: the recording refuses pageable memory with

@@ -42,9 +42,9 @@
  * the same loop, so the result does not depend on the thread count.
  *
  * RMSNorm epilogue (oracle_fused_rmsnorm): the consumers of the q_a / kv_a
- * projections are RMSNorms (TensorRT-LLM PR #20636, Description: "the q_norm /
- * kv_norm RMSNorms"; PR #20502, glm_mla_kv_half_append commit message: RMSNorm of
- * the 512 latent columns of the raw kv_a_proj output).  For a split i with
+ * projections are RMSNorms (TensorRT-LLM PR #20636, Description: q_norm reads wq_a's
+ * output and kv_norm reads wkv's; PR #20502, glm_mla_kv_half_append commit message:
+ * the kv_a_proj output's 512 latent columns, not its RoPE part, are normalised).  For a split i with
  * c_i = norm_cols[i] > 0 and every token m, from the fp64 sums above:
  *
  *   ms[m]  = (1 / c_i) * sum_{r < c_i} y[m][off_i + r]^2          (fp64, increasing r)

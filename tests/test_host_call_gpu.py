@@ -1,7 +1,7 @@
-"""proj_fused_gemm_host through the C ABI: tokens from pinned host memory, outputs back
-to host memory, the projection in between bitwise that of proj_fused_gemm; a bound call
-(HostCall) repeated over several inputs; NULL host pointers refused before anything is
-enqueued."""
+"""proj_fused_gemm_host through the C ABI: tokens from pinned host memory (the staging
+kernel) or pageable memory (a copy-engine copy), outputs back to host memory, the
+projection in between bitwise that of proj_fused_gemm; a bound call (HostCall) repeated
+over several inputs; NULL host pointers refused before anything is enqueued."""
 import ctypes
 
 import pytest
@@ -34,12 +34,40 @@ def test_host_call_matches_device_call(hsp, name, M, tf32):
     calls = [hsp.HostCall(xh, w, wl.splits, outs_host, x_dev, outs_dev, tf32=tf32) for xh in xs]
     for rep in range(2):                      # every bound call twice, in a row
         for xh, call in zip(xs, calls):
+            before = hsp.launch_count()
             call()
             torch.cuda.synchronize()
+            assert hsp.launch_count() == before + 2      # token staging kernel + projection
+            assert torch.equal(x_dev.cpu(), xh)          # the staged tokens, bit for bit
             ref = hsp.fused_gemm(xh.cuda(), w, wl.splits, tf32=tf32)
             hsp.check_device_error()
             for h, r in zip(outs_host, ref):
                 assert torch.equal(h, r.cpu()), (name, M, rep)
+
+
+@pytest.mark.parametrize("name,M", [("wq_a_wkv", 8), ("indexer_fp32", 64)])
+def test_host_call_with_pageable_tokens(hsp, name, M):
+    """Tokens in pageable memory go through a copy-engine copy; outputs in pageable memory
+    come back through the device staging buffers and copies."""
+    wl = W.WORKLOADS[name]
+    w = W.weight_cat(wl).cuda()
+    x_dev = torch.full((M, wl.K), float("nan"), dtype=w.dtype, device="cuda")
+    outs_dev = [torch.empty((M, n), dtype=w.dtype, device="cuda") for n in wl.splits]
+    for pinned_out in (False, True):
+        outs_host = [torch.full((M, n), float("nan"), dtype=w.dtype) for n in wl.splits]
+        if pinned_out:
+            outs_host = [o.pin_memory() for o in outs_host]
+        xh = W.activation(wl, M, 1)
+        assert not xh.is_pinned()
+        before = hsp.launch_count()
+        hsp.HostCall(xh, w, wl.splits, outs_host, x_dev, outs_dev)()
+        torch.cuda.synchronize()
+        assert hsp.launch_count() == before + 1          # the projection only
+        assert torch.equal(x_dev.cpu(), xh)
+        ref = hsp.fused_gemm(xh.cuda(), w, wl.splits)
+        hsp.check_device_error()
+        for h, r in zip(outs_host, ref):
+            assert torch.equal(h, r.cpu()), (name, M, pinned_out)
 
 
 def test_host_call_refuses_null_host_pointers(hsp):

@@ -1,9 +1,9 @@
 """The RMSNorm epilogue (q_norm / kv_norm fused into the projection) against the oracle.
 
 TensorRT-LLM PR #20636, Description: the consumers of wq_a / wkv are the q_norm /
-kv_norm RMSNorms; PR #20502, glm_mla_kv_half_append commit message: RMSNorm of the
-512 latent columns of the raw kv_a_proj output (the 64 RoPE columns are not
-normalized).  Checked here: every normalized output within the bf16 tolerance of the
+kv_norm RMSNorms; PR #20502, glm_mla_kv_half_append commit message: of the kv_a_proj
+output only the 512 latent columns are normalised (its 64 RoPE columns are left
+alone).  Checked here: every normalized output within the bf16 tolerance of the
 oracle's fp64 RMSNorm; the columns and splits left alone bitwise equal to the plain
 fused call; two calls in a row and CUDA-graph replay bitwise equal to eager (the
 workspace's counters are left at zero by every call); argument checks.

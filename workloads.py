@@ -21,8 +21,8 @@ are real checkpoints that are not available here, so every value is drawn):
                 compressed KV 512, k_pe 64) plus the indexer's wk 128 and
                 weights_proj 32 rows appended to the same weight, up to 8 tokens.
   glm_router_fp32
-                the same page, glmRouterGemm commit message: FP32 router logits of
-                256 experts at hidden 6144 for 1 to 16 tokens.
+                the same page, glmRouterGemm commit message: the router's logits in
+                FP32, 256 experts, hidden size 6144, 1-16 tokens.
 
 Recipe: X ~ N(0, 1) and W ~ N(0, 0.02), drawn in fp32 with a CPU
 torch.Generator and rounded once to bf16 (torch's round-to-nearest-even) when
