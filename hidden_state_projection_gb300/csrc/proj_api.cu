@@ -39,6 +39,7 @@ using hsp::LaunchReq;
 using hsp::StreamArgs;
 
 constexpr int kSmemLimit = 232448;          // per-block dynamic shared memory on sm_103
+constexpr int kUmmaSmemBudget = 110 * 1024;  // tensor-memory kernel: ring + receive buffer, two CTAs per SM
 constexpr int kSmemReserve = 1024 + 1024;   // ring alignment slack (1024 for the swizzle) + barriers + flags
 constexpr int kStageWeightBytes = 65536;    // tensor layout: weight bytes per ring stage
 constexpr int kMaxRingStages = 32;
@@ -99,15 +100,16 @@ struct DeviceInfo {
     int cc_ok = 0;
     int *err_word = nullptr;
     int cluster_ctas[17] = {0};  // CTAs co-resident in clusters of 1, 2, 4, 8, 16 (index = size)
+    int pair_ctas[17] = {0};     // the same at two CTAs per SM (the tensor-memory kernel's footprint)
 };
 
-// Shape of the streaming kernels for the co-residency query: one CTA of 288
-// threads and ~200 KB of shared memory per SM.
+// Stand-in kernel for the co-residency query.  Default shape: the streaming kernels,
+// one CTA of 288 threads and ~200 KB of shared memory per SM.
 __global__ void hsp_cluster_probe_kernel(int *p) {
     if (p && threadIdx.x == 0x7fffffff) p[0] = 1;
 }
 
-int co_resident_ctas(int cluster, int fallback) {
+int co_resident_ctas(int cluster, int fallback, int threads = 288, int smem = 200 * 1024) {
     if (cluster > 8 &&
         cudaFuncSetAttribute(hsp_cluster_probe_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -115,8 +117,8 @@ int co_resident_ctas(int cluster, int fallback) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, static_cast<unsigned>(cluster * 16), 1);
-    cfg.blockDim = dim3(288, 1, 1);
-    cfg.dynamicSmemBytes = 200 * 1024;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 1;
@@ -125,7 +127,7 @@ int co_resident_ctas(int cluster, int fallback) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaFuncSetAttribute(hsp_cluster_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+    if (cudaFuncSetAttribute(hsp_cluster_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess ||
         cudaOccupancyMaxActiveClusters(&n, hsp_cluster_probe_kernel, &cfg) != cudaSuccess || n <= 0) {
         (void)cudaGetLastError();
@@ -158,6 +160,8 @@ proj_status device_info(DeviceInfo *out) {
             d.cluster_ctas[4] = co_resident_ctas(4, d.sms);
             d.cluster_ctas[8] = co_resident_ctas(8, d.sms * 3 / 4);
             d.cluster_ctas[16] = co_resident_ctas(16, d.sms * 2 / 3);
+            for (int c = 1; c <= 16; c *= 2)
+                d.pair_ctas[c] = co_resident_ctas(c, d.cluster_ctas[c], hsp::kUmmaThreadsHost, kUmmaSmemBudget);
             void *p = nullptr;
             if ((e = cudaGetSymbolAddress(&p, g_hsp_device_error)) != cudaSuccess)
                 return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
@@ -464,12 +468,21 @@ bool use_umma(int M, proj_dtype dt) {
 
 struct UPlan {
     proj_plan_info info;
-    int compute, NT, S, kb_total, kb_per_slice, tiles, ring, stage_bytes, x_box, smem;
+    int compute, NT, S, TR, kb_total, kb_per_slice, tiles, ring, stage_bytes, x_box, smem;
 };
 
-// K slices and k-blocks per slice depend on (K, dtype) only; the ring is sized
-// so that two CTAs fit on an SM (clusters of eight then pack into the GPCs).
-void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, UPlan *p) {
+// K slices and k-blocks per slice depend on (K, dtype) only (the summation order).  The
+// ring is sized so that two CTAs fit on an SM (the next call's CTAs start beside this
+// call's last ones).  The tile height, the MMA's M, does not change any output bit
+// (tested): 128 weight rows, or 64 for 64-token tiles when all the 64-row tiles times the
+// slices fit one wave at two CTAs per SM (pair_ctas).  Measured on GB300 (µs, 128-row /
+// 64-row tiles, 8 slices): qk_indexer M = 64: 13.8 / 12.1 -- its 24 KB stages left a ring
+// of three beside the 35 KB receive buffer, against five 16 KB stages and 17 KB; wq_a++wkv
+// M = 64: 10.8 / 10.2; but M = 9 / 16 / 32: 10.6 / 11.7, 10.7 / 11.7, 11.3 / 11.7 (qk) and
+// 8.9 / 9.8 (wq_a++wkv): there the twice as many CTAs read the tokens twice as often.
+// Four slices with 64-row tiles and one CTA per SM (36 clusters of 4 fill 144 SMs) were
+// slower still: 14.8 - 15.7 µs for qk_indexer at every M.
+void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_ctas, UPlan *p) {
     memset(p, 0, sizeof *p);
     const int64_t row_bytes = static_cast<int64_t>(K) * elem_size(dt);
     p->compute = dt == PROJ_BF16 ? hsp::kMmaBf16 : hsp::kMmaTf32;
@@ -481,14 +494,16 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, UPlan *p) {
         --p->S;
         p->kb_per_slice = ceil_div(p->kb_total, p->S);
     }
-    p->tiles = ceil_div(n_rows, 128);
+    const int wave = pair_ctas[p->S] > 0 ? pair_ctas[p->S] : pair_ctas[1];
+    p->TR = (p->NT == 64 && ceil_div(n_rows, 64) * p->S <= wave) ? 64 : 128;
+    p->tiles = ceil_div(n_rows, p->TR);
     p->x_box = p->NT * 128;
-    p->stage_bytes = 16384 + p->x_box;
+    p->stage_bytes = p->TR * 128 + p->x_box;
     // receive buffer of the cluster reduction (dedicated); the staging buffer aliases
     // the ring.  Two CTAs per SM: ring + receive buffer within ~110 KB.
-    const int red_bytes = 128 * (p->NT + 4) * 4;
+    const int red_bytes = p->TR * (p->NT + 4) * 4;
     const int recv_bytes = p->S > 1 ? red_bytes : 0;
-    int ring = (110 * 1024 - recv_bytes) / p->stage_bytes;
+    int ring = (kUmmaSmemBudget - recv_bytes) / p->stage_bytes;
     if (ring < 2) ring = 2;
     if (ring > p->kb_per_slice) ring = p->kb_per_slice < 2 ? 2 : p->kb_per_slice;
     while (p->S > 1 && ring * p->stage_bytes < red_bytes) ++ring;
@@ -497,7 +512,7 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, UPlan *p) {
     proj_plan_info &i = p->info;
     i.bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
     i.compute = p->compute;
-    i.rows_per_cta = 128;
+    i.rows_per_cta = p->TR;
     i.row_ctas = p->tiles;
     i.slices = p->S;
     i.k_warps = 1;
@@ -518,10 +533,11 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
                              proj_dtype dt, const hsp::SplitTable &splits, const hsp::PrefetchList &pf,
                              cudaStream_t stream) {
     UPlan p;
-    make_umma_plan(M, K, n_rows, dt, &p);
+    make_umma_plan(M, K, n_rows, dt, dev.pair_ctas, &p);
     hsp::UmmaLaunchReq r{};
     const uint32_t boxk = 128u / static_cast<uint32_t>(elem_size(dt));
-    proj_status st = encode_map(w, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), boxk, 128u, dt, &r.tmap_w);
+    proj_status st = encode_map(w, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), boxk,
+                                static_cast<uint32_t>(p.TR), dt, &r.tmap_w);
     if (st != PROJ_OK) return st;
     st = encode_map(x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), boxk, static_cast<uint32_t>(p.NT), dt,
                     &r.tmap_x);
@@ -880,14 +896,22 @@ proj_status fused_impl(const void *x, const void *w_cat, const int32_t *n_splits
 // host only.  Without a usable device the plan assumes a GB300: 152 SMs, 152 / 152 /
 // 144 / 120 / 112 CTAs co-resident in clusters of 1 / 2 / 4 / 8 / 16.  Leaves the
 // last error string as it was.
-void plan_ctas(int (&ctas)[17]) {
+void plan_ctas(int (&ctas)[17], int (&pairs)[17]) {
+    // GB300 (152 SMs) as measured by the occupancy query, for hosts without the device
     static const int kGb300[17] = {0, 152, 152, 0, 144, 0, 0, 0, 120, 0, 0, 0, 0, 0, 0, 0, 112};
-    for (int k = 0; k < 17; ++k) ctas[k] = kGb300[k];
+    static const int kGb300Pairs[17] = {0, 304, 304, 0, 296, 0, 0, 0, 288, 0, 0, 0, 0, 0, 0, 0, 224};
+    for (int k = 0; k < 17; ++k) {
+        ctas[k] = kGb300[k];
+        pairs[k] = kGb300Pairs[k];
+    }
     char saved[sizeof g_last_error];
     memcpy(saved, g_last_error, sizeof saved);
     DeviceInfo d;
     if (device_info(&d) == PROJ_OK)
-        for (int k = 1; k < 17; ++k) ctas[k] = d.cluster_ctas[k];
+        for (int k = 1; k < 17; ++k) {
+            ctas[k] = d.cluster_ctas[k];
+            pairs[k] = d.pair_ctas[k];
+        }
     else
         (void)cudaGetLastError();
     memcpy(g_last_error, saved, sizeof saved);
@@ -967,8 +991,8 @@ extern "C" {
 
 size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_splits, int32_t num_splits,
                                     const int32_t *norm_cols, proj_dtype dtype) {
-    int ctas[17];
-    plan_ctas(ctas);
+    int ctas[17], pairs[17];
+    plan_ctas(ctas, pairs);
     NormLayout L;
     if (norm_layout(M, K, n_splits, num_splits, norm_cols, dtype, ctas, &L) != PROJ_OK) return 0;
     return L.bytes;
@@ -1247,11 +1271,11 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
     proj_status st = check_shape(M, K, n_rows, dtype);
     if (st != PROJ_OK) return st;
     if (M < 1 || n_rows < 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "M and n_rows must be at least 1");
-    int ctas[17];
-    plan_ctas(ctas);
+    int ctas[17], pairs[17];
+    plan_ctas(ctas, pairs);
     if (use_umma(M, dtype)) {
         UPlan u;
-        make_umma_plan(M, K, n_rows, dtype, &u);
+        make_umma_plan(M, K, n_rows, dtype, pairs, &u);
         *info = u.info;
         return ok();
     }

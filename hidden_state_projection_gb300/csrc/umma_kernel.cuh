@@ -2,27 +2,29 @@
 //
 // Same operation and output scatter as the streaming kernel (TensorRT-LLM PR #20636,
 // Description), for the token counts where the products no longer fit the legacy
-// mma.sync issue rate.  One CTA of four warps owns a 128-row tile of the weight rows
+// mma.sync issue rate.  One CTA of four warps owns a tile of 128 (or 64) weight rows
 // and one K slice; its S K slices form a cluster.
 //
 //   * warps 2-3 first bulk-prefetch the CTA's weight segments (one contiguous run per
 //     row) into L2, so the DRAM sees long runs although the tensor copies below read
 //     128-byte pieces of 128 rows;
 //   * warp 0 lane 0 issues 2-D tensor copies (128-byte swizzle) of the weight box
-//     [128 rows x 128 bytes] and the token box [16/32/64 tokens x 128 bytes] of each
+//     [tile rows x 128 bytes] and the token box [16/32/64 tokens x 128 bytes] of each
 //     k-block into a ring; weight boxes of the first ring's worth of k-blocks go out
 //     before griddepcontrol.wait, token boxes after it (the GLM fused-A order of
 //     TensorRT-LLM PR #20502, glmFusedAGemm commit message);
-//   * warp 1 lane 0 issues four tcgen05.mma (M = 128 weight rows, N = the token tile,
+//   * warp 1 lane 0 issues four tcgen05.mma (M = the tile's weight rows, N = the token tile,
 //     K = 16 bf16 or 8 tf32 each) per k-block into one TMEM accumulator and commits
 //     each stage back to the ring; a final commit marks the accumulator ready;
-//   * all four warps read the accumulator (warp w owns TMEM lanes 32w..32w+31, one
-//     weight row per thread), then either store (S = 1) or stage the partials per
+//   * all four warps read the accumulator (warp w reads TMEM lanes 32w..32w+31: one
+//     weight row per thread, or per lane < 16 for a 64-row tile), then either store
+//     (S = 1) or stage the partials per
 //     owner CTA and bulk-copy each owner's block into its receive buffer (a copy
 //     between cluster shared memories, counted on the owner's mbarrier); the owner
 //     adds the S slices in slice order and stores.  The sum of every
 //     output is the tensor-core accumulation over K in order, then slices in order:
-//     a function of (K, dtype, M bucket) only, never of the row's place in a tile.
+//     a function of (K, dtype, M bucket) only, never of the row's place in a tile or
+//     of the tile's height (64- and 128-row tiles give the same bits, tested).
 //   * the trigger follows a release fence in every storing thread (TensorRT-LLM PR
 //     #20636, Description).
 //
@@ -44,7 +46,6 @@
 namespace hsp {
 
 constexpr int kUmmaThreads = 128;
-constexpr uint32_t kWBoxBytes = 128u * 128u;  // 128 rows x 128 bytes
 
 template <int NT>
 struct UmmaCfg {
@@ -70,11 +71,15 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t ring = smem_u32(smem);
-    constexpr int kPitch = NT + 4;                       // row pitch (floats) of the reduction buffers
-    constexpr uint32_t kRedBytes = 128u * kPitch * 4u;  // one partial per weight row of the tile
+    constexpr int kPitch = NT + 4;  // row pitch (floats) of the reduction buffers
+    // A stage is the weight box [tile rows][128 bytes] followed by the token box, so the
+    // tile height (64 or 128 weight rows, the MMA's M) is what the token box leaves.
+    const uint32_t w_box = a.stage_bytes - a.x_box_bytes;
+    const int TR = static_cast<int>(w_box >> 7);
+    const uint32_t red_bytes = static_cast<uint32_t>(TR) * kPitch * 4u;  // one partial per row of the tile
     const uint32_t ring_bytes = a.ring_stages * a.stage_bytes;
     float *recv = reinterpret_cast<float *>(smem + ring_bytes);  // K-slice partials of my rows (S > 1)
-    const uint32_t recv_bytes = a.slices > 1 ? kRedBytes : 0u;
+    const uint32_t recv_bytes = a.slices > 1 ? red_bytes : 0u;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + ring_bytes + recv_bytes);
     uint64_t *empty = full + a.ring_stages;
     uint64_t *accf = empty + a.ring_stages;
@@ -85,8 +90,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     float *staging = reinterpret_cast<float *>(smem);  // my partials, one block per owner (aliases the ring)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = blockIdx.x * 128;
-    const int rows_here = min(128, a.n_rows - row0);
+    const int row0 = blockIdx.x * TR;
+    const int rows_here = min(TR, a.n_rows - row0);
     const int slice = blockIdx.y;
     const int kb0 = slice * a.kb_per_slice;
     const int nkb = max(0, min(a.kb_total, kb0 + a.kb_per_slice) - kb0);
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         mbar_init(smem_u32(accf), 1);
         mbar_init(smem_u32(recv_bar), 1);
         // every slice's block of my rows arrives on recv_bar: expect all of them now
-        if (a.slices > 1) mbar_arrive_expect_tx(smem_u32(recv_bar), kRedBytes);
+        if (a.slices > 1) mbar_arrive_expect_tx(smem_u32(recv_bar), red_bytes);
         *abort_flag = 0;
         *issued = 0;
         mbar_fence_init();
@@ -110,7 +115,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         for (int i = 0; i < min(nkb, a.ring_stages); ++i) {
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[i]);
-            mbar_expect_tx(fb, kWBoxBytes);
+            mbar_expect_tx(fb, w_box);
             tma_load_2d(ring + i * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb);
         }
     }
@@ -151,7 +156,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[i]);
             mbar_arrive_expect_tx(fb, a.x_box_bytes);
-            tma_load_2d(ring + i * a.stage_bytes + kWBoxBytes, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
+            tma_load_2d(ring + i * a.stage_bytes + w_box, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
             *issued = i + 1;
         }
         for (int i = npre; i < nkb; ++i) {
@@ -164,9 +169,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             }
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[slot]);
-            mbar_arrive_expect_tx(fb, kWBoxBytes + a.x_box_bytes);
+            mbar_arrive_expect_tx(fb, a.stage_bytes);
             tma_load_2d(ring + slot * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb);
-            tma_load_2d(ring + slot * a.stage_bytes + kWBoxBytes, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
+            tma_load_2d(ring + slot * a.stage_bytes + w_box, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
             *issued = i + 1;
         }
     } else if (warp == 1 && lane == 0) {
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         const uint32_t idesc = (1u << 4)                       // D: f32
                                | (kFmt << 7) | (kFmt << 10)    // A, B element type
                                | (static_cast<uint32_t>(NT >> 3) << 17)  // N
-                               | (static_cast<uint32_t>(128 >> 4) << 24); // M
+                               | (static_cast<uint32_t>(TR >> 4) << 24);  // M: the tile's weight rows
         for (int i = 0; i < nkb; ++i) {
             const int slot = i % a.ring_stages;
             const uint32_t par = static_cast<uint32_t>(i / a.ring_stages) & 1u;
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t wa = ring + slot * a.stage_bytes;
-            const uint32_t xa = wa + kWBoxBytes;
+            const uint32_t xa = wa + w_box;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint64_t ad = umma_desc_sw128(wa + k * 32);
@@ -226,8 +231,12 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     }
     __syncthreads();
 
-    // thread (warp w, lane l) owns weight row 32w + l of the tile
-    const int r = warp * 32 + lane;
+    // Warp w reads TMEM lanes 32w .. 32w + 31.  An M = 128 accumulator keeps row i in lane
+    // i; an M = 64 one keeps rows 16w .. 16w + 15 in lanes 32w .. 32w + 15 (the other
+    // sixteen lanes of each quarter hold no rows).  Thread (w, l) owns row w * TR / 4 + l.
+    const int rpw = TR >> 2;
+    const bool has_row = lane < rpw;
+    const int r = warp * rpw + lane;
     float v[NT];
     if (have_acc) {
 #pragma unroll
@@ -248,7 +257,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     bool stored = false;
     constexpr bool kBf16Out = (COMPUTE == kMmaBf16);
     if (a.slices == 1) {
-        if (!aborted && r < rows_here) {
+        if (!aborted && has_row && r < rows_here) {
             const OutRow o = out_row<kBf16Out>(a.splits, row0 + r);
 #pragma unroll
             for (int t = 0; t < NT; ++t)
@@ -262,9 +271,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         // dedicated receive buffer of CTA q, completing on that CTA's receive barrier,
         // which has expected all S blocks since the kernel started.  Each owner waits
         // for its barrier and adds the S slices of its rows in slice order.
-        const int per = 128 / a.slices;
+        const int per = TR / a.slices;
         const uint32_t block_bytes = static_cast<uint32_t>(per * kPitch * 4);
-        {
+        if (has_row) {
             const int q = r / per, rr = r - q * per;
             float *dst = staging + q * per * kPitch + rr * kPitch;
 #pragma unroll

@@ -131,11 +131,14 @@ def test_plan_fits_the_hardware(hsp):
                         assert p["ring_stages"] >= 1
                         assert (p["row_warps"] * p["row_tiles"] * 16) % p["slices"] == 0
                         assert p["threads"] == 288
-                    else:                    # tensor-memory kernel: 128-row tiles, 2 CTAs per SM
+                    else:                    # tensor-memory kernel: 64- or 128-row tiles, 2 CTAs per SM
                         assert M > 8 and dt == 0
-                        assert p["rows_per_cta"] == 128 and p["threads"] == 128
+                        assert p["rows_per_cta"] in (64, 128) and p["threads"] == 128
                         assert p["smem_bytes"] <= 113 * 1024
-                        assert p["ring_stages"] >= 2 and 128 % p["slices"] == 0
+                        assert p["ring_stages"] >= 2 and p["rows_per_cta"] % p["slices"] == 0
+                        if p["rows_per_cta"] == 64:  # 64 tokens; all 64-row tiles in one wave, 2 per SM
+                            assert M > 32
+                            assert p["row_ctas"] * p["slices"] <= {1: 304, 2: 304, 4: 296, 8: 288}[p["slices"]]
 
 
 def test_pack_check_and_options(hsp):

@@ -155,6 +155,21 @@ def test_large_m_engines_match_oracle(hsp, M, forced):
     check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"engine {forced} M{M}")
 
 
+@pytest.mark.parametrize("M", [33, 48, 64])
+def test_tensor_memory_tile_height_keeps_the_bits(hsp, M):
+    """At 33-64 tokens glm_fused_a's 2752 rows run as 128-row tiles when fused (43 tiles of
+    64 over eight K slices would not fit one wave at two CTAs per SM) and each of its
+    splits alone as 64-row tiles: the tile height is the MMA's M and must not change a
+    single output bit (fused = separate), and both agree with the oracle."""
+    wl = W.WORKLOADS["glm_fused_a"]
+    x = W.activation(wl, M)
+    w_cat = W.weight_cat(wl)
+    assert hsp.describe_plan(M, wl.K, wl.n_total, 0)["rows_per_cta"] == 128
+    assert [hsp.describe_plan(M, wl.K, n, 0)["rows_per_cta"] for n in wl.splits] == [64] * len(wl.splits)
+    outs = _run_both(hsp, x, w_cat, wl.splits)
+    check_close(outs, oracle_outputs(x, w_cat, wl.splits), "bf16", f"glm_fused_a M{M}")
+
+
 @pytest.mark.parametrize("M", [1, 2])
 def test_bf16_fma_small_m_path_matches_oracle(hsp, M):
     """The opt-in CUDA-core path for bf16 with one or two tokens."""
