@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kRegThreads, 1)
         mbar_fence_init();
     }
     __syncthreads();
-    if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
+    if (a.trigger_early) griddep_launch_dependents();  // option trigger_early (the tinygemm2 order)
     // The activations are written by the previous kernel on the stream.
     griddep_wait();
     const bool x_issued = a.skip_stage != 0;  // test hook: stage 0 of this kernel is its token copy

@@ -83,7 +83,7 @@ struct StreamArgs {
     uint32_t ring_bytes;       // ring_stages * stage_bytes, at least the reduction buffer
     uint32_t x_off;            // bytes from a stage's start to its first token row
     int32_t skip_stage;        // test hook: this stage of every slice is never loaded (-1: off)
-    int32_t trigger_early;     // test hook: trigger dependents at kernel start
+    int32_t trigger_early;     // option: trigger dependents at kernel start (default: after the stores)
     uint64_t wait_limit_ns;    // bound of every barrier wait
     int *err_word;             // device error word (PROJ_ERR_TIMEOUT on expiry)
     SplitTable splits;
@@ -107,7 +107,7 @@ struct UmmaArgs {
     uint32_t x_box_bytes;      // token rows (16, 32 or 64) * 128
     int32_t prefetch_l2;       // 1: bulk-prefetch the CTA's weight segments into L2 first
     int32_t skip_stage;        // test hook: this k-block of every slice is never loaded (-1: off)
-    int32_t trigger_early;     // test hook: trigger dependents at kernel start
+    int32_t trigger_early;     // option: trigger dependents at kernel start (default: after the stores)
     int32_t pad_;
     uint64_t wait_limit_ns;
     int *err_word;

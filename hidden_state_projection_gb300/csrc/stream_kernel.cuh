@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         }
     }
     __syncthreads();
-    if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
+    if (a.trigger_early) griddep_launch_dependents();  // option trigger_early (the tinygemm2 order)
 
     constexpr bool kFma = (COMPUTE == kFmaFp32 || COMPUTE == kFmaBf16);
     constexpr int kChains = (!kFma && MT == 1) ? 2 : 1;

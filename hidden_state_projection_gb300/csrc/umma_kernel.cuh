@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_d = *tmem_slot;
-    if (a.trigger_early) griddep_launch_dependents();  // test hook (positive control)
+    if (a.trigger_early) griddep_launch_dependents();  // option trigger_early (the tinygemm2 order)
     // First half of a cluster barrier: the peers' receive barriers are initialised
     // before anyone pushes into them (the wait comes after the main loop).  The
     // initialising thread's fence.mbarrier_init.release.cluster, before the CTA

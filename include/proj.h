@@ -99,10 +99,14 @@ typedef struct {
     /* 1: the tensor-memory kernel first prefetches each CTA's weight rows into L2 as
      * contiguous runs.  0 (default): no prefetch (measured slower on GB300). */
     int32_t l2_prefetch;
-    /* Test hook, 0 = off.  1: trigger the dependent launch at kernel start, before any
-     * output store (the order TensorRT-LLM PR #20636, Description, describes for
-     * tinygemm2).  Safe only for consumers that call griddepcontrol.wait; used by the
-     * PDL ordering test as its positive control. */
+    /* 0 (default): the dependent launch is triggered after every output store is
+     * performed.  1: it is triggered at kernel start, before any output store (the order
+     * TensorRT-LLM PR #20636, Description, describes for tinygemm2).  Correct only when
+     * every kernel launched after this one with programmatic stream serialization calls
+     * griddepcontrol.wait before it reads the outputs (all of this library's kernels
+     * do); a dependent that reads without waiting can see stale values, which the PDL
+     * ordering test uses as its positive control.  Measured on GB300 with back-to-back
+     * calls: 0.7-1.5 us less per call (wq_a++wkv M = 8: 5.45 -> 4.60 us). */
     int32_t trigger_early;
     /* bf16 with M <= 2: 0 (default) = mma.sync like 3 <= M <= 8; 1 = fp32 FMA on the
      * CUDA cores.  Both within tolerance, each bitwise self-consistent. */
