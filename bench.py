@@ -60,11 +60,18 @@ SHARED_FILES = ["ptx.cuh", "scatter.cuh", "norm_epilogue.cuh", "prefetch.cuh", "
 
 
 def strip_comments(src: str) -> str:
-    """C/C++ source without // and /* */ comments and blank lines (string literals kept)."""
+    """C/C++ source without // and /* */ comments, blank lines and runs of blanks (string
+    literals kept as they are)."""
     import re
     tok = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
-    code = tok.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", src)
-    return "\n".join(ln.rstrip() for ln in code.splitlines() if ln.strip())
+    code = tok.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", src)
+    out = []
+    for ln in code.splitlines():
+        parts = re.split(r'("(?:\\.|[^"\\])*")', ln)   # odd items are string literals
+        ln = "".join(p if i % 2 else re.sub(r"[ \t]+", " ", p) for i, p in enumerate(parts)).strip()
+        if ln:
+            out.append(ln)
+    return "\n".join(out)
 
 
 def kernel_sources_sha16(kernel: str) -> str:
