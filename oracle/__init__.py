@@ -178,14 +178,28 @@ def cpu_count() -> int:
         return os.cpu_count() or 1
 
 
+# Arm main-ID part numbers of server cores (Arm's technical reference manuals)
+_ARM_PARTS = {"0xd0c": "Neoverse N1", "0xd40": "Neoverse V1", "0xd49": "Neoverse N2",
+              "0xd4f": "Neoverse V2", "0xd84": "Neoverse V3", "0xd8e": "Neoverse N3"}
+
+
 def host_description() -> str:
-    model = ""
+    """CPU model of the host: the x86 model name, or for Arm the core named by its part number."""
+    model, implementer, part = "", "", ""
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu model")):
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model") and not model:
                     model = line.split(":", 1)[1].strip()
-                    break
+                elif key == "cpu implementer" and not implementer:
+                    implementer = line.split(":", 1)[1].strip().lower()
+                elif key == "cpu part" and not part:
+                    part = line.split(":", 1)[1].strip().lower()
     except OSError:
         pass
-    return model or platform.machine()
+    if model:
+        return model
+    if implementer == "0x41" and part:
+        return f"{platform.machine()} {_ARM_PARTS.get(part, 'Arm part ' + part)}"
+    return platform.machine()
