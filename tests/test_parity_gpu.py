@@ -86,6 +86,28 @@ def test_every_token_count(hsp, dtype, tf32):
         check_close(outs, oracle_outputs(x, w_cat, splits), mode_of(dtype, tf32), f"M{M}")
 
 
+@pytest.mark.parametrize("name,tf32", [("wq_a_wkv", False), ("qk_indexer", False), ("glm_fused_a", False),
+                                       ("indexer_fp32", False), ("indexer_fp32", True)])
+def test_every_token_count_full_size(hsp, name, tf32):
+    """Every M from 1 to 64 on a full-size weight of the pages' workloads, so that each
+    switch of the dispatcher is crossed at real K and N: the register ring / streaming /
+    tensor-memory engines at M = 8 | 9, the tcgen05 tile height at 32 | 33 (where it fits
+    one wave), the fp32 GEMV's one-CTA token limit at 6 | 7, the token tiles of every
+    bucket.  All outputs against the oracle, fused and separate bitwise equal."""
+    wl = W.WORKLOADS[name]
+    w_cat = W.weight_cat(wl)
+    wd = w_cat.cuda()
+    for M in range(1, 65):
+        x = W.activation(wl, M, 2)
+        xd = x.cuda()
+        fused = hsp.fused_gemm(xd, wd, wl.splits, tf32=tf32)
+        sep = hsp.separate_gemm(xd, wd, wl.splits, tf32=tf32)
+        hsp.check_device_error()
+        for a, b in zip(fused, sep):
+            assert torch.equal(a, b), (name, M)
+        check_close(fused, oracle_outputs(x, w_cat, wl.splits, threads=16), mode_of(wl.dtype, tf32), f"{name} M{M}")
+
+
 @pytest.mark.parametrize("dtype,tf32", [("bf16", False), ("fp32", False), ("fp32", True)])
 @pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 33, 64])
 def test_small_integers_bit_exact(hsp, dtype, tf32, M):
