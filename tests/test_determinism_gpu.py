@@ -14,9 +14,12 @@ import workloads as W
 
 pytestmark = pytest.mark.gpu
 
+# register ring (wq_a_wkv), tensor memory with 64- and 128-row tiles (qk_indexer 64 / 32),
+# streaming bf16 / fp32 / tf32 (glm_fused_a 5, indexer 16, indexer 64 tf32), fp32 GEMV
+# (indexer 4, router 1)
 CFGS = [("wq_a_wkv_m1", 1, False), ("wq_a_wkv", 8, False), ("qk_indexer", 64, False),
         ("qk_indexer", 32, False), ("glm_fused_a", 5, False), ("indexer_fp32", 16, False),
-        ("indexer_fp32", 64, True)]
+        ("indexer_fp32", 64, True), ("indexer_fp32", 4, False), ("glm_router_fp32", 1, False)]
 
 
 @pytest.fixture(scope="module")
@@ -54,6 +57,21 @@ def test_pdl_on_off_bitwise(hsp, name, M, tf32):
     b = hsp.fused_gemm(x, w, wl.splits, tf32=tf32)
     hsp.set_options(pdl=True)
     assert all(torch.equal(p, q) for p, q in zip(a, b))
+
+
+@pytest.mark.parametrize("name,M,tf32", CFGS)
+def test_trigger_order_bitwise(hsp, name, M, tf32):
+    """The trigger_early option moves only the dependent-launch trigger: same bits."""
+    wl, x, w = _inputs(name, M, 3)
+    a = hsp.fused_gemm(x, w, wl.splits, tf32=tf32)
+    hsp.set_options(pdl=True, trigger_early=True)
+    try:
+        b = hsp.fused_gemm(x, w, wl.splits, tf32=tf32)
+        c = hsp.fused_gemm(x, w, wl.splits, tf32=tf32)   # after an early-triggering call
+    finally:
+        hsp.set_options(pdl=True, trigger_early=False)
+    hsp.check_device_error()
+    assert all(torch.equal(p, q) and torch.equal(p, r) for p, q, r in zip(a, b, c))
 
 
 @pytest.mark.parametrize("separate", [False, True])
