@@ -304,6 +304,17 @@ def time_e2e(hsp, st: Setup, calls: int):
     bound = [hsp.HostCall(xh[c % 4], st.w[c], st.wl.splits, oh, xd, st.outs[c], tf32=st.tf32, stream=stream)
              for c in range(st.copies)]
     us = timed(bound)
+    # The same step with the host waiting for each result before the next step (the
+    # latency a caller sees when step i + 1 needs step i's outputs): host wall clock.
+    n_sync = max(50, min(500, calls // 4))
+    for i in range(st.copies):
+        bound[i]()
+    stream.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n_sync):
+        bound[i % st.copies]()
+        stream.synchronize()
+    sync_us = (time.perf_counter() - t0) * 1e6 / n_sync
     plans = [hsp.HostPlan(xh[c % 4], st.w[c], st.wl.splits, oh, xd, st.outs[c], tf32=st.tf32, stream=stream)
              for c in range(st.copies)]
     plan_us = timed(plans)
@@ -312,7 +323,7 @@ def time_e2e(hsp, st: Setup, calls: int):
     h2d = st.x[0].numel() * st.x[0].element_size()
     d2h = sum(o.numel() * o.element_size() for o in oh)
     del dev
-    return us, h2d, d2h, plan_us
+    return us, h2d, d2h, plan_us, sync_us
 
 
 def cpu_baseline(wl, M, budget_s=12.0):
@@ -361,7 +372,7 @@ def run_ours(args):
     # roofline of one GPU's kernel: its own calls in the (max over ranks) step time
     achieved = bytes_call / (ms_per_step * 1000.0 / args.calls * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
-    e2e_us, h2d, d2h, e2e_plan_us = time_e2e(hsp, st, args.e2e_calls)
+    e2e_us, h2d, d2h, e2e_plan_us, e2e_sync_us = time_e2e(hsp, st, args.e2e_calls)
     # Same calls, each also prefetching the next call's weights into L2 (the cross-kernel
     # weight prefetch of the GLM fused-A kernel): reported beside the headline, not as it.
     gp = capture_graph(hsp, st, args.calls, prefetch_next=True)
@@ -411,7 +422,8 @@ def run_ours(args):
         "e2e": {"value": round(e2e_us, 3), "unit": "µs/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "public API proj_fused_gemm_host per step (bound HostCall): x read from pinned host memory by the token staging kernel, fused call (PDL-chained), outputs stored by the kernel into pinned mapped host memory",
-                "host_plan_us": round(e2e_plan_us, 3)},
+                "host_plan_us": round(e2e_plan_us, 3),
+                "synchronous_step_us": round(e2e_sync_us, 3)},
         "gpu_launches": args.steps * args.calls,   # one fused kernel per call, all inside the graph
         "with_l2_prefetch_of_next_weights": {
             "us_per_call": round(us_pf, 4), "gbs": round(bytes_call / (us_pf * 1e-6) / 1e9, 1),
