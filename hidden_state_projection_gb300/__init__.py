@@ -334,6 +334,28 @@ def fused_gemm_rmsnorm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[in
     return _gemm(fn, x, w_cat, splits, outs, False, stream)
 
 
+def fused_gemm_rmsnorm_static(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
+                              norm_cols: Sequence[int], gammas: Sequence[Optional[torch.Tensor]], eps: float,
+                              outs: Optional[List[torch.Tensor]] = None, stream=None):
+    """fused_gemm_rmsnorm without a workspace argument: proj_fused_gemm_rmsnorm_static uses
+    the library's own fixed device array (for callers that cannot allocate).  Calls that
+    overlap on the GPU race on that array."""
+    if len(norm_cols) != len(splits) or len(gammas) != len(splits):
+        raise ProjError(1, "one norm_cols entry and one gamma per split")
+    for g, c in zip(gammas, norm_cols):
+        if c and (g is None or g.dtype != x.dtype or g.numel() < int(c) or not g.is_contiguous()):
+            raise ProjError(1, "gamma of a normalized split must be a dense tensor of the data type")
+    gp = [g.data_ptr() if (g is not None and c) else 0 for g, c in zip(gammas, norm_cols)]
+
+    def fn(xp, wp, sp, op, M, K, dt, st):
+        ns = (ctypes.c_int32 * len(sp))(*[int(v) for v in sp])
+        nc = (ctypes.c_int32 * len(norm_cols))(*[int(v) for v in norm_cols])
+        gpa = (ctypes.c_void_p * len(gp))(*[int(p) if p else None for p in gp])
+        po = (ctypes.c_void_p * len(op))(*[int(p) for p in op])
+        _check(lib().proj_fused_gemm_rmsnorm_static(xp, wp, ns, len(sp), nc, gpa, float(eps), po, M, K, dt, st))
+    return _gemm(fn, x, w_cat, splits, outs, False, stream)
+
+
 def separate_gemm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
                   outs: Optional[List[torch.Tensor]] = None, tf32: bool = False, stream=None):
     """One launch per split over its rows of w_cat; bitwise equal to fused_gemm."""
@@ -341,12 +363,21 @@ def separate_gemm(x: torch.Tensor, w_cat: torch.Tensor, splits: Sequence[int],
 
 
 def pack_weights(ws: Sequence[torch.Tensor], w_cat: Optional[torch.Tensor] = None, stream=None):
-    """Row-concatenate weights into w_cat on the device; returns (w_cat, views of it)."""
+    """Row-concatenate weights into w_cat on the device (one copy kernel; parts that
+    already are their own rows of w_cat are skipped); returns (w_cat, views of it).
+    Passing the same w_cat again refreshes it in place, e.g. after a reload."""
+    if not ws:
+        raise ProjError(1, "at least one weight is required")
     K = ws[0].shape[1]
     dt = ws[0].dtype
+    for w in ws:
+        if w.dim() != 2 or w.shape[1] != K or w.dtype != dt or not w.is_contiguous():
+            raise ProjError(1, "weights must be dense 2-D tensors with the same K and dtype")
     n_rows = [int(w.shape[0]) for w in ws]
     if w_cat is None:
         w_cat = torch.empty((sum(n_rows), K), dtype=dt, device=ws[0].device)
+    elif w_cat.shape != (sum(n_rows), K) or w_cat.dtype != dt or not w_cat.is_contiguous():
+        raise ProjError(1, f"w_cat must be a dense [{sum(n_rows)}, {K}] {dt} tensor")
     code = dtype_code(w_cat)
     ptrs = (ctypes.c_void_p * len(ws))(*[w.data_ptr() for w in ws])
     ns = (ctypes.c_int32 * len(ws))(*n_rows)

@@ -9,12 +9,12 @@ namespace hsp {
 cudaError_t launch_gemv(const GemvLaunchReq &r) {
     auto kern = hsp_gemv_kernel;
     constexpr int kMaxDev = 64;
-    static std::atomic<unsigned char> configured[kMaxDev];
+    static std::atomic<uint64_t> configured[kMaxDev];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    if (!configured[dev].load(std::memory_order_acquire)) {
+    if (!set_up_in_current_context(configured[dev])) {
         // the opt-in limit covers static and dynamic shared memory together
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, kern);
@@ -22,7 +22,7 @@ cudaError_t launch_gemv(const GemvLaunchReq &r) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  232448 - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
-        configured[dev].store(1, std::memory_order_release);
+        configured[dev].store(current_context_id(), std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = r.grid;

@@ -12,12 +12,12 @@ template <bool NORM>
 cudaError_t launch_reg_variant(const RegLaunchReq &r) {
     auto kern = hsp_reg_kernel<kRegDepth, NORM>;
     constexpr int kMaxDev = 64;
-    static std::atomic<unsigned char> configured[kMaxDev];
+    static std::atomic<uint64_t> configured[kMaxDev];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    if (!configured[dev].load(std::memory_order_acquire)) {
+    if (!set_up_in_current_context(configured[dev])) {
         // the opt-in limit covers static and dynamic shared memory together
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, kern);
@@ -25,7 +25,7 @@ cudaError_t launch_reg_variant(const RegLaunchReq &r) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  232448 - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
-        configured[dev].store(1, std::memory_order_release);
+        configured[dev].store(current_context_id(), std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = r.grid;

@@ -13,15 +13,15 @@ constexpr int kMaxDev = 64;
 template <int COMPUTE, int NT>
 cudaError_t launch_umma_variant(const UmmaLaunchReq &r) {
     auto kern = hsp_umma_kernel<COMPUTE, NT>;
-    static std::atomic<unsigned char> configured[kMaxDev];
+    static std::atomic<uint64_t> configured[kMaxDev];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-    if (!configured[dev].load(std::memory_order_acquire)) {
+    if (!set_up_in_current_context(configured[dev])) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (e != cudaSuccess) return e;
-        configured[dev].store(1, std::memory_order_release);
+        configured[dev].store(current_context_id(), std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = r.grid;

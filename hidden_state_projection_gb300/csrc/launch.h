@@ -4,9 +4,22 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "stream_args.h"
 
 namespace hsp {
+
+// Id of the CUDA context current on the calling thread (0: none yet); proj_api.cu.
+uint64_t current_context_id();
+
+// Per-device set-up (a kernel's shared-memory opt-in) is recorded as the id of the
+// context it was made in: true when that is the current context.  A reset device or
+// another context on it gets the set-up again.
+inline bool set_up_in_current_context(const std::atomic<uint64_t> &slot) {
+    const uint64_t ctx = current_context_id();
+    return ctx != 0 && slot.load(std::memory_order_acquire) == ctx;
+}
 
 struct LaunchReq {
     int compute;     // Compute
@@ -70,6 +83,17 @@ constexpr int kGemvMaxTokenBytes = 192 * 1024;
 // Token staging for the host entry point: n16 16-byte chunks from `src` (the device
 // address of page-locked host memory) to `dst`, at most max_ctas CTAs, PDL-chained.
 cudaError_t launch_stage(const void *src, void *dst, int64_t n16, int max_ctas, int pdl, cudaStream_t stream);
+
+// Weight packer: part p's n16 chunks run from src[p] to chunk dst16[p] of W_cat; the
+// parts are laid end to end in the launch (first16[p] = chunks before part p,
+// first16[count] = all chunks).  One launch, at most max_ctas CTAs, no PDL attribute.
+struct PackArgs {
+    int32_t count;
+    const uint4 *src[kMaxSplits];
+    int64_t dst16[kMaxSplits];
+    int64_t first16[kMaxSplits + 1];
+};
+cudaError_t launch_pack(void *dst, const PackArgs &a, int max_ctas, cudaStream_t stream);
 
 // Threads per CTA of a bucket (eight consumer warps + one producer warp).
 constexpr int kThreadsPerCta = 9 * 32;

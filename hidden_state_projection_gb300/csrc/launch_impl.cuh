@@ -14,13 +14,13 @@ constexpr int kMaxDynamicSmem = 232448;  // 227 KiB, the per-block opt-in limit 
 template <int COMPUTE, int MT, int RT, int WR, int WK, bool TENSOR, bool NORM>
 cudaError_t launch_one(const LaunchReq &r) {
     auto kern = hsp_stream_kernel<COMPUTE, MT, RT, WR, WK, TENSOR, NORM>;
-    // The shared-memory opt-in is per function and per device; set it once.
-    static std::atomic<unsigned char> configured[kMaxDevices];
+    // The shared-memory opt-in is per function and per context; set it once in each.
+    static std::atomic<uint64_t> configured[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!configured[dev].load(std::memory_order_acquire)) {
+    if (!set_up_in_current_context(configured[dev])) {
         // the opt-in limit covers static and dynamic shared memory together
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, kern);
@@ -31,7 +31,7 @@ cudaError_t launch_one(const LaunchReq &r) {
         // clusters of 16 K slices (fp32 rows with many tokens) exceed the portable 8
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
-        configured[dev].store(1, std::memory_order_release);
+        configured[dev].store(current_context_id(), std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = r.grid;

@@ -139,14 +139,53 @@ int co_resident_ctas(int cluster, int fallback, int threads = 288, int smem = 20
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
 bool g_dev_ready[64] = {};
+uint64_t g_dev_ctx[64] = {};  // context the entry of g_dev was made in
+
+}  // namespace
+
+namespace hsp {
+// Unique id of the CUDA context current on the calling thread, 0 when none is current
+// (or the driver cannot tell).  Device addresses of this library's __device__ symbols
+// belong to one context: a reset device (cudaDeviceReset) or another context on the
+// same device gets new ones, so every per-device cache of such an address is keyed by
+// this id as well.
+uint64_t current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess) {
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+        } else {
+            (void)cudaGetLastError();
+        }
+    });
+    if (!get_cur || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_cur(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? static_cast<uint64_t>(id) : 0;
+}
+}  // namespace hsp
+
+namespace {
 
 proj_status device_info(DeviceInfo *out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(PROJ_ERR_DEVICE, "device ordinal %d out of range", dev);
+    // No current context yet (first call, or right after a reset) counts as a change:
+    // the lookup below creates it, and the entry is then tagged with its id.
+    const uint64_t ctx = hsp::current_context_id();
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_dev_ready[dev]) {
+    if (!g_dev_ready[dev] || ctx == 0 || ctx != g_dev_ctx[dev]) {
         DeviceInfo d;
         int major = 0, minor = 0;
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
@@ -169,6 +208,7 @@ proj_status device_info(DeviceInfo *out) {
         }
         g_dev[dev] = d;
         g_dev_ready[dev] = true;
+        g_dev_ctx[dev] = hsp::current_context_id();
     }
     *out = g_dev[dev];
     if (!out->cc_ok)
@@ -998,10 +1038,16 @@ size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_split
     return L.bytes;
 }
 
-proj_status proj_fused_gemm_rmsnorm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+}  // extern "C"
+
+namespace hsp {
+// proj_fused_gemm_rmsnorm, optionally clearing the workspace's split counters (its
+// first 256 bytes) on the stream right before the kernel, once every argument has been
+// checked: a refused call enqueues nothing.
+proj_status fused_gemm_rmsnorm_impl(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
                                     const int32_t *norm_cols, const void *const *gammas, float eps,
                                     void *const *outs, int32_t M, int32_t K, proj_dtype dtype, void *workspace,
-                                    size_t workspace_bytes, proj_stream_t stream) {
+                                    size_t workspace_bytes, bool clear_counters, proj_stream_t stream) {
     int64_t n_total = 0;
     proj_status st = validate(x, w_cat, n_splits, num_splits, outs, M, K, dtype, &n_total);
     if (st != PROJ_OK) return st;
@@ -1040,10 +1086,26 @@ proj_status proj_fused_gemm_rmsnorm(const void *x, const void *w_cat, const int3
     }
     hsp::PrefetchList none;
     memset(&none, 0, sizeof none);
+    if (clear_counters) {
+        const cudaError_t e = cudaMemsetAsync(workspace, 0, L.vals_at, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace counters (cudaMemsetAsync)");
+    }
     st = launch_rows(dev, x, w_cat, static_cast<int>(n_total), M, K, dtype, t, none,
                      reinterpret_cast<cudaStream_t>(stream), a.active ? &a : nullptr);
     return st == PROJ_OK ? ok() : st;
 }
+}  // namespace hsp
+
+extern "C" {
+
+proj_status proj_fused_gemm_rmsnorm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                                    const int32_t *norm_cols, const void *const *gammas, float eps,
+                                    void *const *outs, int32_t M, int32_t K, proj_dtype dtype, void *workspace,
+                                    size_t workspace_bytes, proj_stream_t stream) {
+    return hsp::fused_gemm_rmsnorm_impl(x, w_cat, n_splits, num_splits, norm_cols, gammas, eps, outs, M, K, dtype,
+                                        workspace, workspace_bytes, false, stream);
+}
+
 
 proj_status proj_fused_gemm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
                             void *const *outs, int32_t M, int32_t K, proj_dtype dtype, proj_stream_t stream) {
@@ -1232,20 +1294,49 @@ proj_status proj_separate_gemm(const void *x, const void *w_cat, const int32_t *
 proj_status proj_pack_weights(const void *const *ws, const int32_t *n_rows, int32_t num, int32_t K,
                               proj_dtype dtype, void *w_cat, proj_stream_t stream) {
     if (!dtype_valid(dtype)) return fail(PROJ_ERR_UNSUPPORTED_DTYPE, "dtype %d is not PROJ_BF16/FP32/TF32", (int)dtype);
-    if (!ws || !n_rows || !w_cat || num < 1 || K < 1) return fail(PROJ_ERR_INVALID_ARG, "bad pack arguments");
+    if (!ws || !n_rows || !w_cat) return fail(PROJ_ERR_INVALID_ARG, "ws, n_rows and w_cat must not be NULL");
+    if (num < 1 || num > PROJ_MAX_SPLITS)
+        return fail(PROJ_ERR_INVALID_ARG, "num=%d (1..%d weights per pack)", num, PROJ_MAX_SPLITS);
+    if (K < 1) return fail(PROJ_ERR_INVALID_ARG, "K=%d (need at least 1)", K);
     const size_t pitch = static_cast<size_t>(K) * elem_size(dtype);
+    if (pitch % 16 != 0)
+        return fail(PROJ_ERR_MISALIGNED, "rows of K=%d elements are %zu bytes, not a multiple of 16", K, pitch);
+    if (!aligned16(w_cat)) return fail(PROJ_ERR_MISALIGNED, "w_cat must be 16-byte aligned");
+    size_t total_rows = 0;
+    for (int i = 0; i < num; ++i) {
+        if (n_rows[i] < 0) return fail(PROJ_ERR_INVALID_ARG, "n_rows[%d]=%d is negative", i, n_rows[i]);
+        if (n_rows[i] == 0) continue;  // nothing to read: any pointer, NULL included
+        if (!ws[i]) return fail(PROJ_ERR_INVALID_ARG, "ws[%d] is NULL", i);
+        if (!aligned16(ws[i])) return fail(PROJ_ERR_MISALIGNED, "ws[%d] must be 16-byte aligned", i);
+        total_rows += static_cast<size_t>(n_rows[i]);
+    }
+    // W_cat occupies [lo, hi).  A source inside that range is either exactly its own
+    // rows (already packed: nothing to copy) or refused: the copy would read rows that
+    // this or an earlier part overwrites.
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(w_cat), hi = lo + total_rows * pitch;
+    hsp::PackArgs a;
+    memset(&a, 0, sizeof a);
     size_t off = 0;
     for (int i = 0; i < num; ++i) {
-        if (!ws[i] || n_rows[i] < 0) return fail(PROJ_ERR_INVALID_ARG, "ws[%d] / n_rows[%d] invalid", i, i);
-        char *dst = static_cast<char *>(w_cat) + off * pitch;
         const size_t bytes = static_cast<size_t>(n_rows[i]) * pitch;
-        if (bytes && dst != ws[i]) {
-            cudaError_t e = cudaMemcpyAsync(dst, ws[i], bytes, cudaMemcpyDeviceToDevice,
-                                            reinterpret_cast<cudaStream_t>(stream));
-            if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (pack)");
-        }
+        const uintptr_t src = reinterpret_cast<uintptr_t>(ws[i]), dst = lo + off * pitch;
         off += static_cast<size_t>(n_rows[i]);
+        if (bytes == 0 || src == dst) continue;
+        if (src < hi && src + bytes > lo)
+            return fail(PROJ_ERR_INVALID_ARG, "ws[%d] overlaps w_cat without being its own rows [%zu, %zu)", i,
+                        off - n_rows[i], off);
+        a.src[a.count] = reinterpret_cast<const uint4 *>(ws[i]);
+        a.dst16[a.count] = static_cast<int64_t>((dst - lo) / 16);
+        a.first16[a.count + 1] = a.first16[a.count] + static_cast<int64_t>(bytes / 16);
+        ++a.count;
     }
+    if (a.count == 0) return ok();  // every part already is its own rows
+    DeviceInfo dev;
+    proj_status st = device_info(&dev);
+    if (st != PROJ_OK) return st;
+    cudaError_t e = hsp::launch_pack(w_cat, a, dev.sms * 4, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return ok();
 }
 

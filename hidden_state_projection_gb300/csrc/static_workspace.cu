@@ -9,12 +9,13 @@
 // fixed array compiled into the library instead and allocates nothing.
 //
 // The array lives in device memory of every GPU that loads this library, for the
-// life of the process.  Host code cannot use its name as a device address; its
-// address is looked up once per device (cudaGetSymbolAddress, with that device
-// current) on the first call made with that device current.
+// life of the process.  Host code cannot use its name as a device address: the
+// address is looked up (cudaGetSymbolAddress, with the device current) on the first
+// call made in a context, and again whenever the current context is not the one the
+// address was looked up in (a device reset with cudaDeviceReset, or another context
+// on the same device, gives the array a new address).
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -22,7 +23,12 @@
 
 namespace hsp {
 proj_status set_last_error(proj_status st, const char *msg);  // proj_api.cu
-}
+uint64_t current_context_id();                                // proj_api.cu
+proj_status fused_gemm_rmsnorm_impl(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+                                    const int32_t *norm_cols, const void *const *gammas, float eps,
+                                    void *const *outs, int32_t M, int32_t K, proj_dtype dtype, void *workspace,
+                                    size_t workspace_bytes, bool clear_counters, proj_stream_t stream);
+}  // namespace hsp
 
 namespace {
 
@@ -36,19 +42,22 @@ static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspa
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_addr[kMaxDevices] = {nullptr};
+uint64_t g_addr_ctx[kMaxDevices] = {0};  // context each address was looked up in
 
-// Device address of g_static_workspace on the current device (looked up once).
+// Device address of g_static_workspace in the current context.
 cudaError_t workspace_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const uint64_t ctx = hsp::current_context_id();
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_addr[dev]) {
+    if (!g_addr[dev] || ctx == 0 || ctx != g_addr_ctx[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_workspace);
         if (e != cudaSuccess) return e;
         g_addr[dev] = p;
+        g_addr_ctx[dev] = hsp::current_context_id();  // the lookup made a context current if none was
     }
     *out = g_addr[dev];
     return cudaSuccess;
@@ -79,13 +88,8 @@ extern "C" proj_status proj_fused_gemm_rmsnorm_static(const void *x, const void 
         return hsp::set_last_error(PROJ_ERR_CUDA, msg);
     }
     // Every call shares the array and finds the previous call's contents there: the
-    // split counters must start at zero, so they are cleared on the caller's stream.
-    e = cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        std::snprintf(msg, sizeof msg, "proj_fused_gemm_rmsnorm_static: clearing the counters: %s",
-                      cudaGetErrorString(e));
-        return hsp::set_last_error(PROJ_ERR_CUDA, msg);
-    }
-    return proj_fused_gemm_rmsnorm(x, w_cat, n_splits, num_splits, norm_cols, gammas, eps, outs, M, K, dtype, ws,
-                                   kStaticWorkspaceBytes, stream);
+    // split counters must start at zero, so the call clears them on the caller's
+    // stream, after every argument check and right before its kernel.
+    return hsp::fused_gemm_rmsnorm_impl(x, w_cat, n_splits, num_splits, norm_cols, gammas, eps, outs, M, K, dtype, ws,
+                                        kStaticWorkspaceBytes, true, stream);
 }

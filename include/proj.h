@@ -236,13 +236,18 @@ size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_split
  * a fixed 1 MiB array compiled into this library, present in the memory of every GPU
  * that loads it until the process exits.  The caller still passes inputs and outputs,
  * with the meaning and limits of proj_fused_gemm_rmsnorm.
- *   - The first call made with a given device current looks up the array's device
- *     address on that device (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *   - The first call made in a context looks up the array's device address there
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.  A
+ *     device reset (cudaDeviceReset) or another context on the device gives the array
+ *     a new address, which the next call in that context looks up again (so that call,
+ *     too, belongs outside a capture).
  *   - Every call shares the one array and finds the last call's contents in it; each
- *     call clears the part that must start at zero (cudaMemsetAsync on `stream`)
- *     before its kernel.  Calls that overlap on the GPU race on the array: issue
- *     them on one stream, or order them.
+ *     call clears the part that must start at zero (cudaMemsetAsync of 256 bytes on
+ *     `stream`, enqueued after every argument check, so a refused call enqueues
+ *     nothing) before its kernel.  That memset sits between the previous kernel on the
+ *     stream and this call's kernel, so the kernel cannot overlap its predecessor by
+ *     programmatic dependent launch.  Calls that overlap on the GPU race on the
+ *     array: issue them on one stream, or order them.
  *   - Shapes whose workspace (proj_rmsnorm_workspace_bytes) exceeds 1 MiB are refused
  *     with PROJ_ERR_UNSUPPORTED_SHAPE and a message that gives both sizes.
  */
@@ -312,10 +317,25 @@ proj_status proj_separate_gemm(const void *x, const void *w_cat, const int32_t *
 /*
  * proj_pack_weights -- build W_cat by copying the projection weights one after
  * another (TensorRT-LLM PR #20636, Description: post_load_weights copies wq_a and
- * wkv into one row-concatenated tensor).  ws[i] is a device [n_rows[i], K] dense
- * matrix; w_cat receives them in order.  Device-to-device copies enqueued on
- * `stream`; re-running it into the same w_cat refreshes the weights in place.
- * ws[i] may already alias its rows of w_cat (the copy is then skipped).
+ * wkv into one row-concatenated tensor and rebinds the per-projection weights as
+ * views of it).  ws[i] is a device [n_rows[i], K] dense matrix; w_cat receives them
+ * in order, rows [sum_{j<i} n_rows[j], sum_{j<=i} n_rows[j]).
+ *   ws       host array of num device pointers, each 16-byte aligned (may be NULL
+ *            where n_rows[i] == 0)
+ *   n_rows   host [num], each >= 0 (a part of 0 rows copies nothing)
+ *   num      1..PROJ_MAX_SPLITS
+ *   K        elements per row; K * element size must be a multiple of 16 bytes
+ *            (PROJ_ERR_MISALIGNED otherwise, like the projection calls)
+ *   w_cat    device, 16-byte aligned, owned by the caller and at least
+ *            sum(n_rows) * K elements long: the library cannot check the size of
+ *            the caller's buffer, so a shorter one is overrun
+ * One copy kernel enqueued on `stream` (none when every part is skipped), without
+ * programmatic dependent launch: it starts after earlier work on the stream and a
+ * projection call enqueued after it reads the new weights.  Re-running it into the
+ * same w_cat refreshes the weights in place (a checkpoint reload).  A ws[i] that is
+ * exactly its own rows of w_cat (already packed, or a view written through) is
+ * skipped; a ws[i] that overlaps w_cat anywhere else is refused with
+ * PROJ_ERR_INVALID_ARG before anything is enqueued.
  */
 proj_status proj_pack_weights(const void *const *ws, const int32_t *n_rows, int32_t num,
                               int32_t K, proj_dtype dtype, void *w_cat, proj_stream_t stream);

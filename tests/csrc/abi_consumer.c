@@ -4,7 +4,8 @@
  * the CUDA runtime's C API).
  *
  *   abi_consumer host    queries and argument checks that need no GPU (exit 0 on success)
- *   abi_consumer device  one fused and one separate call on small-integer bf16 data,
+ *   abi_consumer device  W_cat packed from three weights (proj_pack_weights), then one
+ *                        fused and one separate call on small-integer bf16 data,
  *                        checked element by element against a double loop written here
  *                        (entries in {-1, 0, 1} and K = 192: every partial sum is an
  *                        integer of magnitude at most 192, exact in fp32 and in bf16)
@@ -55,6 +56,18 @@ static int host_checks(void) {
     check(proj_fused_gemm(NULL, (void *)0x20000, splits, 2, outs, 1, 64, PROJ_BF16, NULL) == PROJ_ERR_INVALID_ARG,
           "NULL x refused");
     check(strlen(proj_last_error_string()) > 0, "the last refusal has a message");
+    {
+        /* the packer's refusals happen on the host, before anything is enqueued */
+        const void *parts[2] = {(const void *)0x50000, (const void *)0x60000};
+        const void *inside[2] = {(const void *)(0x20000 + 8 * 128), (const void *)0x60000};
+        const int32_t rows[2] = {16, 8};
+        check(proj_pack_weights(parts, rows, 2, 60, PROJ_BF16, (void *)0x20000, NULL) == PROJ_ERR_MISALIGNED,
+              "pack: 120-byte rows refused");
+        check(proj_pack_weights(inside, rows, 2, 64, PROJ_BF16, (void *)0x20000, NULL) == PROJ_ERR_INVALID_ARG,
+              "pack: a source inside w_cat that is not its own rows refused");
+        check(proj_pack_weights(parts, rows, 9, 64, PROJ_BF16, (void *)0x20000, NULL) == PROJ_ERR_INVALID_ARG,
+              "pack: more parts than PROJ_MAX_SPLITS refused");
+    }
     return failures == 0 ? 0 : 1;
 }
 
@@ -92,7 +105,26 @@ static int device_checks(void) {
     for (s = 0; s < NS; ++s)
         if (cudaMalloc(&douts[s], sizeof(uint16_t) * M * splits[s]) != cudaSuccess) return 2;
     cudaMemcpy(dx, x, sizeof(uint16_t) * M * K, cudaMemcpyHostToDevice);
-    cudaMemcpy(dw, w, sizeof(uint16_t) * N * K, cudaMemcpyHostToDevice);
+    /* W_cat is packed by the library from three separately allocated weights */
+    {
+        void *dparts[NS] = {NULL, NULL, NULL};
+        const void *cparts[NS];
+        uint16_t *back = malloc(sizeof(uint16_t) * N * K);
+        if (!back) return 2;
+        off = 0;
+        for (s = 0; s < NS; ++s) {
+            if (cudaMalloc(&dparts[s], sizeof(uint16_t) * splits[s] * K) != cudaSuccess) return 2;
+            cudaMemcpy(dparts[s], w + (size_t)off * K, sizeof(uint16_t) * splits[s] * K, cudaMemcpyHostToDevice);
+            cparts[s] = dparts[s];
+            off += splits[s];
+        }
+        check(proj_pack_weights(cparts, splits, NS, K, PROJ_BF16, dw, NULL) == PROJ_OK, "proj_pack_weights");
+        check(cudaDeviceSynchronize() == cudaSuccess, "device synchronise after the pack");
+        cudaMemcpy(back, dw, sizeof(uint16_t) * N * K, cudaMemcpyDeviceToHost);
+        check(memcmp(back, w, sizeof(uint16_t) * N * K) == 0, "packed w_cat is the row concatenation");
+        for (s = 0; s < NS; ++s) cudaFree(dparts[s]);
+        free(back);
+    }
     for (path = 0; path < 2; ++path) {
         const proj_status st = path == 0 ? proj_fused_gemm(dx, dw, splits, NS, douts, M, K, PROJ_BF16, NULL)
                                          : proj_separate_gemm(dx, dw, splits, NS, douts, M, K, PROJ_BF16, NULL);

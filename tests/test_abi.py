@@ -197,6 +197,44 @@ def test_pack_check_and_options(hsp):
     hsp.set_options(pdl=True)
 
 
+def _pack(hsp, ws, n_rows, K=64, dtype=0, w_cat=0x7F0000000000, num=None):
+    ptrs = (ctypes.c_void_p * max(1, len(ws)))(*ws)
+    ns = (ctypes.c_int32 * max(1, len(n_rows)))(*n_rows)
+    return hsp.lib().proj_pack_weights(ptrs, ns, len(ws) if num is None else num, K, dtype, w_cat, None)
+
+
+def test_pack_refusals(hsp):
+    """proj_pack_weights checks its arguments on the host before anything is enqueued
+    (TensorRT-LLM PR #20636, Description: the packed tensor is the weights' row
+    concatenation, so a source inside W_cat other than its own rows cannot be copied)."""
+    S = hsp.STATUS
+    base, K = 0x7F0000000000, 64
+    pitch = K * 2
+    a, b = 0x7E0000000000, 0x7E0000100000
+    before = hsp.launch_count()
+    assert _pack(hsp, [a, b], [16, 8], dtype=9) == S["PROJ_ERR_UNSUPPORTED_DTYPE"]
+    assert _pack(hsp, [a, b], [16, 8], K=60) == S["PROJ_ERR_MISALIGNED"]           # 120-byte rows
+    assert _pack(hsp, [a, b], [16, 8], K=62, dtype=1) == S["PROJ_ERR_MISALIGNED"]  # 248-byte rows
+    assert _pack(hsp, [a, b], [16, 8], w_cat=base + 8) == S["PROJ_ERR_MISALIGNED"]
+    assert _pack(hsp, [a + 4, b], [16, 8]) == S["PROJ_ERR_MISALIGNED"]
+    assert _pack(hsp, [a, 0], [16, 8]) == S["PROJ_ERR_INVALID_ARG"]
+    assert _pack(hsp, [a, b], [16, -1]) == S["PROJ_ERR_INVALID_ARG"]
+    assert _pack(hsp, [a, b], [16, 8], K=0) == S["PROJ_ERR_INVALID_ARG"]
+    assert _pack(hsp, [a] * 9, [1] * 9) == S["PROJ_ERR_INVALID_ARG"]
+    assert _pack(hsp, [], [], num=0) == S["PROJ_ERR_INVALID_ARG"]
+    assert _pack(hsp, [a, b], [16, 8], w_cat=0) == S["PROJ_ERR_INVALID_ARG"]
+    # sources inside W_cat that are not their own rows: refused, whatever the overlap
+    assert _pack(hsp, [base + 16 * pitch, b], [16, 8]) == S["PROJ_ERR_INVALID_ARG"]   # ws[0] on ws[1]'s rows
+    assert _pack(hsp, [a, base + 8 * pitch], [16, 8]) == S["PROJ_ERR_INVALID_ARG"]    # ws[1] straddles both
+    assert _pack(hsp, [base - 8 * pitch, b], [16, 8]) == S["PROJ_ERR_INVALID_ARG"]    # ends inside W_cat
+    assert "overlaps w_cat" in hsp.lib().proj_last_error_string().decode()
+    # just below and just past W_cat: no overlap; every part its own rows: nothing to do
+    assert _pack(hsp, [base, base + 16 * pitch], [16, 8]) == S["PROJ_OK"]
+    assert _pack(hsp, [base, b], [16, 0]) == S["PROJ_OK"]                              # empty part skipped
+    assert _pack(hsp, [base, 0], [16, 0]) == S["PROJ_OK"]                              # ... even as NULL
+    assert hsp.launch_count() == before
+
+
 def test_prefetch_entry_validation(hsp):
     import ctypes
     S = hsp.STATUS
