@@ -27,8 +27,15 @@ def as_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to(torch.float64).cpu().numpy()
 
 
+# Largest element error as a fraction of the allowed band, per checked case and mode
+# (printed at the end of the test session by conftest.py), so that a regression that
+# still fits inside a band is visible.
+MARGINS = []
+
+
 def check_close(gpu_outs, ref_outs, mode: str, what: str = ""):
-    """mode: 'bf16' | 'fp32' | 'tf32'."""
+    """mode: 'bf16' | 'fp32' | 'tf32'.  Returns the largest error / band over all outputs."""
+    worst = 0.0
     for i, (g, r) in enumerate(zip(gpu_outs, ref_outs)):
         g = as_f64(g)
         assert g.shape == r.shape, (what, i, g.shape, r.shape)
@@ -43,11 +50,15 @@ def check_close(gpu_outs, ref_outs, mode: str, what: str = ""):
             nrm = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
             assert nrm <= TF32_ROWMAX_REL, f"{what} split {i}: normwise {nrm:.3e}"
         err = np.abs(g - r)
+        if err.size:
+            worst = max(worst, float(np.max(err / bound)))
         bad = err > bound
         if bad.any():
             idx = np.argwhere(bad)[:5]
             detail = ", ".join(f"[{a},{b}] gpu={g[a, b]!r} ref={r[a, b]!r}" for a, b in idx)
             raise AssertionError(f"{what} split {i}: {int(bad.sum())}/{bad.size} outside tolerance; {detail}")
+    MARGINS.append((mode, what, worst))
+    return worst
 
 
 def mode_of(dtype: str, tf32: bool) -> str:

@@ -120,15 +120,21 @@ def _pow2_expr(s: str) -> float:
 
 
 def test_golden_rounding_cases(oracle_mod):
+    """Hand-derived bit patterns at rounding boundaries, bf16 and fp32 outputs: ties to
+    even in both directions, no double rounding, signs, subnormals, overflow."""
     cases = json.load(open(os.path.join(GOLDEN, "rounding_cases.json")))["cases"]
+    assert sum(c.get("dtype", "bf16") == "fp32" for c in cases) >= 6
     for c in cases:
+        fp32 = c.get("dtype", "bf16") == "fp32"
         x = torch.tensor([[_pow2_expr(s) for s in c["x"]]], dtype=torch.float64)
         w = torch.tensor([[_pow2_expr(s) for s in c["w"]]], dtype=torch.float64)
-        xb, wb = x.to(torch.bfloat16), w.to(torch.bfloat16)
-        # the inputs must be exact in bf16 for the case to mean what it says
+        tdt = torch.float32 if fp32 else torch.bfloat16
+        xb, wb = x.to(tdt), w.to(tdt)
+        # the inputs must be exact in the dtype for the case to mean what it says
         assert torch.equal(xb.to(torch.float64), x) and torch.equal(wb.to(torch.float64), w), c["name"]
-        (out,) = oracle_mod.fused(_bits(xb), _bits(wb), [1], oracle_mod.BF16)
-        assert int(out[0, 0]) == int(c["expect_bits"], 16), c["name"]
+        (out,) = oracle_mod.fused(_bits(xb), _bits(wb), [1], oracle_mod.FP32 if fp32 else oracle_mod.BF16)
+        got = int(np.asarray(out).view(np.uint32)[0, 0]) if fp32 else int(out[0, 0])
+        assert got == int(c["expect_bits"], 16), (c["name"], hex(got))
 
 
 # ---------------------------------------------------------------- closed forms

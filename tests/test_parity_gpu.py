@@ -51,7 +51,7 @@ def test_workload_full_size(hsp, name, M, tf32):
     x = W.activation(wl, M)
     w_cat = W.weight_cat(wl)
     outs = _run_both(hsp, x, w_cat, wl.splits, tf32)
-    check_close(outs, oracle_outputs(x, w_cat, wl.splits), mode_of(wl.dtype, tf32), name)
+    check_close(outs, oracle_outputs(x, w_cat, wl.splits), mode_of(wl.dtype, tf32), f"{name} M{M}")
 
 
 EDGE = [
