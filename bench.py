@@ -197,6 +197,27 @@ def job_us_per_call(ms_per_step: float, calls_per_rank: int, world_size: int) ->
     return ms_per_step * 1000.0 / (calls_per_rank * world_size)
 
 
+# ---------------------------------------------------------------- the workload's config
+
+def workload_config(wl, M: int, tf32: bool, ws: int) -> dict:
+    """The `config` object of both arms: what is computed, not how it is timed."""
+    dt = wl.dtype + ("/tf32" if tf32 else "")
+    return {
+        "workload": f"{wl.name}: X[{M},{wl.K}] {dt} . W_cat[{wl.n_total},{wl.K}]^T, splits "
+                    f"{list(wl.splits)} ({'+'.join(wl.split_names)}), fused call",
+        "M": M, "K": wl.K, "n_total": wl.n_total, "splits": list(wl.splits),
+        "l2_policy": "at least 16 distinct weight copies cycled per call, together more than 3x L2",
+        "parallelism": f"replicas x{ws}",
+    }
+
+
+# The metric's token counts beside the headline (wq_a++wkv at M = 8): the configs that
+# quote M = 1 and M = 64, and the others at the ends of their token ranges.
+PER_M = (("wq_a_wkv_m1", 1, False), ("wq_a_wkv", 8, False), ("qk_indexer", 64, False))
+MORE_CONFIGS = (("qk_indexer", 1, False), ("glm_fused_a", 1, False), ("glm_fused_a", 8, False),
+                ("indexer_fp32", 64, False), ("indexer_fp32", 64, True), ("indexer_fp32", 16, False))
+
+
 # ---------------------------------------------------------------- our arm
 
 class Setup:
@@ -346,6 +367,69 @@ def cpu_baseline(wl, M, budget_s=12.0):
                       f"{oracle.host_description()})"}
 
 
+def time_rmsnorm_variants(hsp, dev, calls, steps, warmup):
+    """µs per call of the RMSNorm-epilogue call at wq_a++wkv M = 8 (q_norm / kv_norm on
+    both splits), with a caller workspace and with the library's fixed array (whose
+    per-call counter clear is a memset between the kernels), same rotation as above."""
+    wl, M, cols = W.WORKLOADS["wq_a_wkv"], 8, (1280, 512)
+    st = Setup(wl, M, dev)
+    g0 = torch.Generator().manual_seed(3)
+    gam = [(1.0 + 0.1 * torch.randn(c, generator=g0)).to(torch.bfloat16).to(dev) for c in cols]
+    ws_t = torch.zeros(hsp.rmsnorm_workspace_bytes(M, wl.K, wl.splits, cols), dtype=torch.uint8, device=dev)
+    res = {}
+    for label, static in (("caller_workspace_us", False), ("static_workspace_us", True)):
+        def one(c):
+            if static:
+                hsp.fused_gemm_rmsnorm_static(st.x[c], st.w[c], wl.splits, cols, gam, 1e-6, outs=st.outs[c])
+            else:
+                hsp.fused_gemm_rmsnorm(st.x[c], st.w[c], wl.splits, cols, gam, 1e-6, ws_t, outs=st.outs[c])
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for c in range(st.copies):
+                one(c)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(calls):
+                one(i % st.copies)
+        tot, _ = time_graph(g, steps, warmup)
+        res[label] = round(tot * 1000.0 / (steps * calls), 4)
+        del g
+    res["how"] = ("proj_fused_gemm_rmsnorm (caller workspace) and proj_fused_gemm_rmsnorm_static (built-in "
+                  "array, a 256-byte memset before each kernel) at wq_a++wkv M=8, norm on both splits")
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_config(hsp, wl, M, tf32, dev, calls, steps, warmup, barrier, ws):
+    """µs per call and the HBM roofline of one more config, timed like the headline."""
+    st = Setup(wl, M, dev, tf32=tf32)
+    g = capture_graph(hsp, st, calls)
+    total_ms, _ = time_graph(g, steps, warmup, barrier)
+    del g
+    ms_step = max_over_ranks(total_ms / steps, dev) if ws > 1 else total_ms / steps
+    us_gpu = ms_step * 1000.0 / calls
+    peak, _ = measured_peaks()
+    b = st.bytes_per_call()
+    achieved = b / (us_gpu * 1e-6) / 1e9
+    kernel = hsp.describe_plan(M, wl.K, wl.n_total, hsp.PROJ_TF32 if tf32 else
+                               (hsp.PROJ_BF16 if wl.dtype == "bf16" else hsp.PROJ_FP32))["engine"]
+    out = {"us_per_call": round(job_us_per_call(ms_step, calls, ws), 4), "bytes_per_call": b,
+           "gpu_launches": steps * calls,
+           "achieved_gbs": round(achieved, 1), "frac": round(achieved / peak, 4),
+           "engine": ENGINE_NAMES.get(kernel, str(kernel)), "weight_copies": st.copies,
+           "config": workload_config(wl, M, tf32, ws)}
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
+ENGINE_NAMES = {0: "streaming", 1: "tcgen05", 2: "register ring", 3: "fp32 register GEMV"}
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     import hidden_state_projection_gb300 as hsp
@@ -364,6 +448,21 @@ def run_ours(args):
     g = capture_graph(hsp, st, args.calls)
     with ClockSampler(local) as clk:
         total_ms, per = time_graph(g, args.steps, args.warmup, barrier)
+        del g
+        hsp.check_device_error()
+        # the metric's other token counts, same rotation, graph length and clocks
+        per_m, more = {}, {}
+        if not args.headline_only:
+            for dest, table in ((per_m, PER_M), (more, MORE_CONFIGS)):
+                for wname, m, tf in table:
+                    if (wname, m, tf) == (name, M, args.tf32):
+                        continue
+                    dest[f"{wname} M={m}{' tf32' if tf else ''}"] = time_config(
+                        hsp, W.WORKLOADS[wname], m, tf, dev, args.calls, max(3, args.steps // 2), args.warmup,
+                        barrier, ws)
+        rms = None
+        if not args.headline_only and ws == 1:
+            rms = time_rmsnorm_variants(hsp, dev, args.calls, max(3, args.steps // 2), args.warmup)
     hsp.check_device_error()
     ms_per_step = max_over_ranks(total_ms / args.steps, dev) if ws > 1 else total_ms / args.steps
     # whole job: every rank ran args.calls calls per step, all within ms_per_step
@@ -403,16 +502,12 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else ("tf32" if args.tf32 else "f32"),
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights; shapes of the pages' projections)",
-        "config": {
-            "workload": f"{name}: X[{M},{wl.K}] {wl.dtype} . W_cat[{wl.n_total},{wl.K}]^T, splits "
-                        f"{list(wl.splits)} ({'+'.join(wl.split_names)}), fused call",
-            "M": M, "K": wl.K, "n_total": wl.n_total, "splits": list(wl.splits),
-            "calls_per_step": args.calls, "weight_copies": st.copies,
-            "l2_policy": f"{st.copies} distinct weight copies cycled per call "
-                         f"({st.copies * wl.weight_bytes() / 1e6:.0f} MB > 3x L2)",
-            "timing": "CUDA-graph replay of calls_per_step calls per step, CUDA events",
-            "pdl": not args.no_pdl, "parallelism": f"replicas x{ws}",
-        },
+        "config": workload_config(wl, M, args.tf32, ws),
+        "timing": {"calls_per_step": args.calls, "weight_copies": st.copies,
+                   "weight_bytes_cycled": st.copies * wl.weight_bytes(),
+                   "how": "CUDA-graph replay of calls_per_step calls per step, CUDA events on the "
+                          "launching stream; weights past L2 by rotation (inputs larger than L2)",
+                   "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": args.traffic if args.traffic is not None else profiled_traffic(name, M),
@@ -437,6 +532,14 @@ def run_ours(args):
         "clocks": clocks,
         "step_ms_min": round(min(per), 5), "step_ms_median": round(statistics.median(per), 5),
     }
+    if per_m:
+        headline = {"us_per_call": line["value"], "bytes_per_call": bytes_call, "achieved_gbs": round(achieved, 1),
+                    "frac": round(achieved / peak, 4), "headline": True}
+        line["per_M"] = {f"{name} M={M}{' tf32' if args.tf32 else ''}": headline, **per_m}
+        line["more_configs"] = more
+    if rms:
+        line["rmsnorm_epilogue"] = rms
+
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, M, args.cpu_seconds)
     if rank == 0:
@@ -471,8 +574,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(us, 2), "unit": "µs/call",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1000, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": f"{args.workload}: X[{M},{wl.K}] . W_cat[{wl.n_total},{wl.K}]^T, fused",
-                                         "M": M, "splits": list(wl.splits)},
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights; shapes of the pages' projections)",
+        "config": workload_config(wl, M, args.tf32, ws),
         "cpu_baseline": {"value": round(us, 2), "unit": "µs/call", "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} full calls (one per step) on {cores} threads, {oracle.host_description()}"},
         "e2e": {"value": round(us, 2), "unit": "µs/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -549,6 +652,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of this kernel (reported as is)")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the headline workload only (no per_M / more_configs entries)")
     args = ap.parse_args()
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps >= 1 and --warmup >= 0")

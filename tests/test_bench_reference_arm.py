@@ -32,3 +32,14 @@ def test_reference_line_has_the_driver_keys():
 
 def test_reference_arm_prints_on_rank_zero_only():
     assert _run({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"}, "--workload", "indexer_fp32", "--M", "1") == []
+
+
+def test_reference_config_is_the_gpu_arms_config():
+    """Both arms describe the same workload with the same config object (bench.py builds
+    both from workload_config), so the driver can pair their lines."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    (line,) = _run(None, "--workload", "wq_a_wkv", "--M", "8")
+    assert line["config"] == bench.workload_config(W.WORKLOADS["wq_a_wkv"], 8, False, 1)
+    assert "tf32" in bench.workload_config(W.WORKLOADS["indexer_fp32"], 64, True, 1)["workload"]
