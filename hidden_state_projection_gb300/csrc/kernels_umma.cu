@@ -21,6 +21,9 @@ cudaError_t launch_umma_variant(const UmmaLaunchReq &r) {
     if (!set_up_in_current_context(configured[dev])) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
         if (e != cudaSuccess) return e;
+        // clusters of 16 K slices (tf32 rows of 16 KB and more) exceed the portable 8
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
         configured[dev].store(current_context_id(), std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};

@@ -500,9 +500,15 @@ proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0,
 // wave.  The tensor-memory kernel has no such cliff, so it takes every M >= 9; option
 // large_m_path 1 / 2 forces one of them.
 constexpr int kStreamMaxM = 8;
+// PROJ_TF32 runs the tensor-memory kernel (kind::tf32, the fp32 operands read as tf32)
+// only when large_m_path is 2.  Measured on GB300 (µs, streaming mma.sync / tcgen05 over
+// 16 K slices): indexer 192 x 7168 at M = 1 / 4 / 16 / 64: 5.37 / 9.12, 5.60 / 9.61,
+// 5.91 / 9.61, 9.48 / 9.90; router 256 x 6144 at M = 1 / 4 / 16: 5.54 / 9.07, 5.58 /
+// 9.09, 6.40 / 9.07.  So the streaming kernel stays the default at every M.
 bool use_umma(int M, proj_dtype dt) {
-    if (M <= 8 || dt != PROJ_BF16) return false;
     const int o = g_opt_large_m_path.load();
+    if (dt == PROJ_TF32) return o == 2;
+    if (M <= 8 || dt != PROJ_BF16) return false;
     return o == 2 || (o == 0 && M > kStreamMaxM);
 }
 
@@ -529,13 +535,20 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_cta
     p->NT = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     p->kb_total = static_cast<int>((row_bytes + 127) / 128);
     p->S = p->kb_total >= 64 ? 8 : (p->kb_total >= 32 ? 4 : (p->kb_total >= 8 ? 2 : 1));
+    // tf32 rows are twice as long in bytes; their projections (the indexer's 192 rows,
+    // the router's 256) have few rows: sixteen slices of the long rows give the grid
+    // enough CTAs.  A function of (K, dtype) only, like every slice count.
+    if (dt == PROJ_TF32 && p->kb_total >= 128) p->S = 16;
     p->kb_per_slice = ceil_div(p->kb_total, p->S);
     while (p->S > 1 && (p->S - 1) * p->kb_per_slice >= p->kb_total) {
         --p->S;
         p->kb_per_slice = ceil_div(p->kb_total, p->S);
     }
     const int wave = pair_ctas[p->S] > 0 ? pair_ctas[p->S] : pair_ctas[1];
-    p->TR = (p->NT == 64 && ceil_div(n_rows, 64) * p->S <= wave) ? 64 : 128;
+    // 64-row tiles: at 64 tokens when they fit one wave, and whenever 128-row tiles
+    // would leave more than half of the SMs (pair_ctas[1] / 2 of them) without a CTA.
+    const bool few = ceil_div(n_rows, 128) * p->S * 4 <= pair_ctas[1];
+    p->TR = ((p->NT == 64 || few) && ceil_div(n_rows, 64) * p->S <= wave) ? 64 : 128;
     p->tiles = ceil_div(n_rows, p->TR);
     p->x_box = p->NT * 128;
     p->stage_bytes = p->TR * 128 + p->x_box;
@@ -1038,16 +1051,10 @@ size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_split
     return L.bytes;
 }
 
-}  // extern "C"
-
-namespace hsp {
-// proj_fused_gemm_rmsnorm, optionally clearing the workspace's split counters (its
-// first 256 bytes) on the stream right before the kernel, once every argument has been
-// checked: a refused call enqueues nothing.
-proj_status fused_gemm_rmsnorm_impl(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
+proj_status proj_fused_gemm_rmsnorm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
                                     const int32_t *norm_cols, const void *const *gammas, float eps,
                                     void *const *outs, int32_t M, int32_t K, proj_dtype dtype, void *workspace,
-                                    size_t workspace_bytes, bool clear_counters, proj_stream_t stream) {
+                                    size_t workspace_bytes, proj_stream_t stream) {
     int64_t n_total = 0;
     proj_status st = validate(x, w_cat, n_splits, num_splits, outs, M, K, dtype, &n_total);
     if (st != PROJ_OK) return st;
@@ -1086,24 +1093,9 @@ proj_status fused_gemm_rmsnorm_impl(const void *x, const void *w_cat, const int3
     }
     hsp::PrefetchList none;
     memset(&none, 0, sizeof none);
-    if (clear_counters) {
-        const cudaError_t e = cudaMemsetAsync(workspace, 0, L.vals_at, reinterpret_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace counters (cudaMemsetAsync)");
-    }
     st = launch_rows(dev, x, w_cat, static_cast<int>(n_total), M, K, dtype, t, none,
                      reinterpret_cast<cudaStream_t>(stream), a.active ? &a : nullptr);
     return st == PROJ_OK ? ok() : st;
-}
-}  // namespace hsp
-
-extern "C" {
-
-proj_status proj_fused_gemm_rmsnorm(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
-                                    const int32_t *norm_cols, const void *const *gammas, float eps,
-                                    void *const *outs, int32_t M, int32_t K, proj_dtype dtype, void *workspace,
-                                    size_t workspace_bytes, proj_stream_t stream) {
-    return hsp::fused_gemm_rmsnorm_impl(x, w_cat, n_splits, num_splits, norm_cols, gammas, eps, outs, M, K, dtype,
-                                        workspace, workspace_bytes, false, stream);
 }
 
 

@@ -191,7 +191,9 @@ __global__ void __launch_bounds__(kRegThreads, 1)
             }
         }
     }
-    if constexpr (NORM) stored |= norm_epilogue<true, kRegMaxRows, 8>(a, sums, finish, row0, rows_here, aborted, tid);
+    if constexpr (NORM)
+        stored |= norm_epilogue<true, kRegMaxRows, 8>(a, sums, finish, row0, rows_here, aborted, tid, &part[0][0][0],
+                                                      kRegWarps * kRegMaxRows * 8);
 
     if (aborted && tid == 0 && x_issued) {
         // the token copy may still be in flight: let it land before the CTA leaves

@@ -24,10 +24,6 @@
 namespace hsp {
 proj_status set_last_error(proj_status st, const char *msg);  // proj_api.cu
 uint64_t current_context_id();                                // proj_api.cu
-proj_status fused_gemm_rmsnorm_impl(const void *x, const void *w_cat, const int32_t *n_splits, int32_t num_splits,
-                                    const int32_t *norm_cols, const void *const *gammas, float eps,
-                                    void *const *outs, int32_t M, int32_t K, proj_dtype dtype, void *workspace,
-                                    size_t workspace_bytes, bool clear_counters, proj_stream_t stream);
 }  // namespace hsp
 
 namespace {
@@ -87,9 +83,10 @@ extern "C" proj_status proj_fused_gemm_rmsnorm_static(const void *x, const void 
         std::snprintf(msg, sizeof msg, "proj_fused_gemm_rmsnorm_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         return hsp::set_last_error(PROJ_ERR_CUDA, msg);
     }
-    // Every call shares the array and finds the previous call's contents there: the
-    // split counters must start at zero, so the call clears them on the caller's
-    // stream, after every argument check and right before its kernel.
-    return hsp::fused_gemm_rmsnorm_impl(x, w_cat, n_splits, num_splits, norm_cols, gammas, eps, outs, M, K, dtype, ws,
-                                        kStaticWorkspaceBytes, true, stream);
+    // Every call shares the array and finds the previous call's contents there.  Only
+    // the arrival counters and abort flags (the first 256 bytes) must start at zero: a
+    // __device__ array is zero when the library is loaded, and every call, one that gave
+    // up a wait included, leaves them at zero again.  So nothing is cleared per call.
+    return proj_fused_gemm_rmsnorm(x, w_cat, n_splits, num_splits, norm_cols, gammas, eps, outs, M, K, dtype, ws,
+                                   kStaticWorkspaceBytes, stream);
 }

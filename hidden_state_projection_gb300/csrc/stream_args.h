@@ -49,7 +49,7 @@ struct NormArgs {
     int32_t cta_count[kMaxSplits];  // CTAs holding normalized rows of split i
     float *vals;                    // workspace
     float *partial;                 // workspace
-    unsigned *counter;              // workspace, [kMaxSplits], zero between calls
+    unsigned *counter;              // workspace: [kMaxSplits] arrivals, [kMaxSplits] abort flags; zero between calls
 };
 
 // K is cut into units of 128 bytes.  Unit u is summed by warp (u mod WK) of the

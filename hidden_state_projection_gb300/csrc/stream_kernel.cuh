@@ -642,7 +642,9 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
         }
     }
     if constexpr (NORM)
-        stored |= norm_epilogue<kBf16Out, kSlots, kXP>(a, red, armed + a.ring_stages, row0, rows_here, aborted, tid);
+        stored |= norm_epilogue<kBf16Out, kSlots, kXP>(a, red, armed + a.ring_stages, row0, rows_here, aborted, tid,
+                                                       red + kSlots * kXP,
+                                                       static_cast<int>(a.ring_bytes / 4) - kSlots * kXP);
 
     if (a.slices > 1) {
         // ---- K slices of the cluster added in slice order ----

@@ -93,8 +93,10 @@ typedef struct {
     int32_t skip_stage_plus1;
     /* Kernel for bf16 with 9 <= M <= 64: 0 (default) and 2 = the tensor-memory kernel
      * (tcgen05.mma into TMEM); 1 = the streaming mma.sync kernel (the one that also
-     * serves M <= 8, tf32 and fp32).  Both give results within tolerance; each is
-     * bitwise self-consistent (fused = separate, run to run). */
+     * serves M <= 8, tf32 and fp32).  For PROJ_TF32 at every M: 0 (default) and 1 = the
+     * streaming kernel, 2 = the tensor-memory kernel (kind::tf32; slower on GB300 for
+     * the pages' tf32 shapes).  All give results within tolerance; each is bitwise
+     * self-consistent (fused = separate, run to run). */
     int32_t large_m_path;
     /* 1: the tensor-memory kernel first prefetches each CTA's weight rows into L2 as
      * contiguous runs.  0 (default): no prefetch (measured slower on GB300). */
@@ -207,9 +209,9 @@ proj_status proj_fused_gemm_prefetch(const void *x, const void *w_cat, const int
  *   eps        finite, >= 0
  *   workspace  device, 16-byte aligned, at least proj_rmsnorm_workspace_bytes(...)
  *              bytes, owned by the caller.  Zero it once before its first use; every
- *              call leaves it ready for the next (its counters back at zero).  Calls
- *              that share a workspace must not overlap on the GPU.  After a call that
- *              reported PROJ_ERR_TIMEOUT, zero it again.
+ *              call, one that reported PROJ_ERR_TIMEOUT included, leaves it ready for
+ *              the next (its counters back at zero).  Calls that share a workspace
+ *              must not overlap on the GPU.
  * PROJ_BF16 with 1 <= M <= 8 only (PROJ_ERR_UNSUPPORTED_DTYPE / _SHAPE otherwise).
  * Bitwise identical run to run and under CUDA-graph replay.
  */
@@ -241,13 +243,12 @@ size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_split
  *     device reset (cudaDeviceReset) or another context on the device gives the array
  *     a new address, which the next call in that context looks up again (so that call,
  *     too, belongs outside a capture).
- *   - Every call shares the one array and finds the last call's contents in it; each
- *     call clears the part that must start at zero (cudaMemsetAsync of 256 bytes on
- *     `stream`, enqueued after every argument check, so a refused call enqueues
- *     nothing) before its kernel.  That memset sits between the previous kernel on the
- *     stream and this call's kernel, so the kernel cannot overlap its predecessor by
- *     programmatic dependent launch.  Calls that overlap on the GPU race on the
- *     array: issue them on one stream, or order them.
+ *   - Every call shares the one array and finds the last call's contents in it.  The
+ *     part that must start at zero (the arrival counters) is zero when the library is
+ *     loaded, and every call, one that reported PROJ_ERR_TIMEOUT included, leaves it at
+ *     zero; nothing is cleared per call, so a call is one kernel launch, chained to the
+ *     previous kernel on the stream like proj_fused_gemm_rmsnorm.  Calls that overlap
+ *     on the GPU race on the array: issue them on one stream, or order them.
  *   - Shapes whose workspace (proj_rmsnorm_workspace_bytes) exceeds 1 MiB are refused
  *     with PROJ_ERR_UNSUPPORTED_SHAPE and a message that gives both sizes.
  */

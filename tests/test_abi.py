@@ -132,13 +132,15 @@ def test_plan_fits_the_hardware(hsp):
                         assert (p["row_warps"] * p["row_tiles"] * 16) % p["slices"] == 0
                         assert p["threads"] == 288
                     else:                    # tensor-memory kernel: 64- or 128-row tiles, 2 CTAs per SM
-                        assert M > 8 and dt == 0
+                        assert (M > 8 and dt == 0) or dt == 2      # bf16 above 8 tokens; tf32 at every M
                         assert p["rows_per_cta"] in (64, 128) and p["threads"] == 128
                         assert p["smem_bytes"] <= 113 * 1024
                         assert p["ring_stages"] >= 2 and p["rows_per_cta"] % p["slices"] == 0
-                        if p["rows_per_cta"] == 64:  # 64 tokens; all 64-row tiles in one wave, 2 per SM
-                            assert M > 32
-                            assert p["row_ctas"] * p["slices"] <= {1: 304, 2: 304, 4: 296, 8: 288}[p["slices"]]
+                        if p["rows_per_cta"] == 64:  # all 64-row tiles in one wave at 2 per SM, and
+                            # 64 tokens, or 128-row tiles would leave most SMs idle
+                            assert M > 32 or -(-n // 128) * p["slices"] * 4 <= 304
+                            assert -(-n // 64) * p["slices"] <= {1: 304, 2: 304, 4: 296, 8: 288, 16: 224}[p["slices"]]
+
 
 
 def test_pack_check_and_options(hsp):
@@ -188,7 +190,12 @@ def test_pack_check_and_options(hsp):
     assert hsp.describe_plan(64, 7168, 192, 1)["smem_bytes"] == 6 * 7168 * 4
     hsp.set_options(reg_path=0)
     assert [hsp.describe_plan(M, 6144, 256, 1)["engine"] for M in (1, 8)] == [3, 3]
-    assert hsp.describe_plan(1, 7168, 192, 2)["engine"] == 0
+    # tf32: the streaming mma.sync kernel by default; large_m_path 2: the tensor-memory kernel (kind::tf32)
+    assert [hsp.describe_plan(M, 7168, 192, 2)["engine"] for M in (1, 8, 9, 64)] == [0, 0, 0, 0]
+    hsp.set_options(large_m_path=2)
+    assert [hsp.describe_plan(M, 7168, 192, 2)["engine"] for M in (1, 8, 9, 64)] == [1, 1, 1, 1]
+    assert hsp.describe_plan(64, 7168, 192, 2)["slices"] == 16
+    hsp.set_options(large_m_path=0)
     assert hsp.describe_plan(1, 8196, 192, 1)["engine"] == 0            # K past 8192
     hsp.set_options(reg_path=1)
     assert hsp.describe_plan(1, 7168, 192, 1)["engine"] == 0

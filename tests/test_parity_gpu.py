@@ -250,3 +250,23 @@ def test_fp32_register_gemv_and_streaming_match_oracle(hsp, K, splits, reg_path)
             check_close(outs, oracle_outputs(x, w_cat, splits), "fp32", f"reg_path {reg_path} K{K} M{M}")
     finally:
         hsp.set_options(pdl=True, reg_path=0)
+
+
+@pytest.mark.parametrize("name", ["indexer_fp32", "glm_router_fp32"])
+@pytest.mark.parametrize("forced", [1, 2])
+def test_tf32_engines_match_oracle(hsp, name, forced):
+    """PROJ_TF32 runs the streaming mma.sync kernel by default (large_m_path 1 too);
+    large_m_path 2 takes the tensor-memory kernel (kind::tf32, sixteen K slices of these
+    long fp32 rows).  Both meet the tf32 tolerance at the workload's full size, fused
+    and separate."""
+    wl = W.WORKLOADS[name]
+    w_cat = W.weight_cat(wl)
+    hsp.set_options(pdl=True, large_m_path=forced)
+    try:
+        for M in (1, 5, 16, 40, 64):
+            assert hsp.describe_plan(M, wl.K, wl.n_total, 2)["engine"] == (0 if forced == 1 else 1)
+            x = W.activation(wl, M, 5)
+            outs = _run_both(hsp, x, w_cat, wl.splits, tf32=True)
+            check_close(outs, oracle_outputs(x, w_cat, wl.splits), "tf32", f"{name} engine {forced} M{M}")
+    finally:
+        hsp.set_options(pdl=True, large_m_path=0)

@@ -131,3 +131,30 @@ def test_rmsnorm_argument_checks(hsp):
     outs = hsp.fused_gemm_rmsnorm(x, w, wl.splits, (1280, 512), gam, EPS, ws)
     hsp.check_device_error()
     assert all(torch.isfinite(o.float()).all() for o in outs)
+
+
+@pytest.mark.parametrize("name,M,norm_cols", [CASES[2], CASES[4]])
+def test_rmsnorm_workspace_reusable_after_timeout(hsp, name, M, norm_cols):
+    """A call whose waits run out (the test hook leaves one stage unloaded in every CTA)
+    reports PROJ_ERR_TIMEOUT; every CTA still arrives on its split's counter, so the
+    same workspace, not zeroed again, gives the bits of a fresh workspace next."""
+    import hidden_state_projection_gb300 as m
+    wl = W.WORKLOADS[name]
+    x, w = W.activation(wl, M, 6).cuda(), W.weight_cat(wl).cuda()
+    gam = _gammas(norm_cols, 19)
+    fresh, _ = _run(hsp, x, w, wl.splits, norm_cols, gam)
+    hsp.check_device_error()
+    ws = torch.zeros(hsp.rmsnorm_workspace_bytes(M, wl.K, wl.splits, norm_cols), dtype=torch.uint8, device="cuda")
+    hsp.set_options(pdl=True, wait_limit_us=20000, skip_stage=0)
+    try:
+        _run(hsp, x, w, wl.splits, norm_cols, gam, ws=ws)
+        with pytest.raises(m.ProjError) as ei:
+            hsp.check_device_error()
+        assert ei.value.status_name == "PROJ_ERR_TIMEOUT"
+    finally:
+        hsp.set_options(pdl=True, wait_limit_us=0, skip_stage=None)
+    assert int(torch.count_nonzero(ws[:256])) == 0          # counters and abort flags back at zero
+    for _ in range(2):
+        again, _ = _run(hsp, x, w, wl.splits, norm_cols, gam, ws=ws)
+        hsp.check_device_error()
+        assert all(torch.equal(a, b) for a, b in zip(again, fresh))
