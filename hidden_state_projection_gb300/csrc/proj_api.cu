@@ -305,9 +305,10 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     p->RT = p->R > p->WR * 16 ? 2 : 1;
     const int slots = p->WR * p->RT * 16;
     p->grid_x = ceil_div(n_rows, p->R);
-    // partial sums of the warps, plus (K slices) the receive buffer of the cluster
-    // reduction; rows of 8 * MT + 1 floats (the kernel pads them against bank conflicts)
-    const int red_bytes = (p->WK * slots + (p->S > 1 ? slots : 0)) * (8 * p->MT + 1) * 4;
+    // partial sums of the warps
+    // (rows of 8 * MT + 1 floats, padded against bank conflicts), plus (K slices) the
+    // staging and receive blocks of the cluster reduction (rows of 8 * MT + 4 floats)
+    const int red_bytes = p->WK * slots * (8 * p->MT + 1) * 4 + (p->S > 1 ? 2 * slots * (8 * p->MT + 4) * 4 : 0);
     const int budget = kSmemLimit - kSmemReserve;
     const int Us = p->units_per_slice;
     p->tensor = (row_bytes % hsp::kUnitBytes) == 0;
@@ -374,8 +375,8 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     p->ring_bytes = p->ring_stages * p->stage_bytes;
     if (p->ring_bytes < red_bytes) p->ring_bytes = red_bytes;
     p->ring_bytes = ceil_div(p->ring_bytes, 128) * 128;
-    // ring, full/empty barriers, abort flag, armed[ring], RMSNorm flags[8], slack
-    p->smem = 1024 + p->ring_bytes + 2 * p->ring_stages * 8 + 8 + 4 * p->ring_stages + 4 * hsp::kMaxSplits + 64;
+    // ring, full/empty barriers, receive barrier, abort flag, armed[ring], RMSNorm flags[8], slack
+    p->smem = 1024 + p->ring_bytes + 2 * p->ring_stages * 8 + 8 + 8 + 4 * p->ring_stages + 4 * hsp::kMaxSplits + 64;
     proj_plan_info &i = p->info;
     i.bucket = p->bucket;
     i.compute = p->compute;

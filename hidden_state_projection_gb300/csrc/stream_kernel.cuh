@@ -303,6 +303,10 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     // slots, so that a warp reading one token of 32 consecutive rows hits 32 banks (with
     // a pitch of 8 * MT the combine loop read one bank 8- to 32-fold).
     constexpr int kXP = kXRows + 1;
+    // Row pitch of the K-slice reduction's staging and receive blocks: a multiple of
+    // four floats, so that each owner's block is a whole number of 16-byte chunks (the
+    // unit of a bulk copy between cluster shared memories).
+    constexpr int kSP = kXRows + 4;
 
     // The ring starts on a 1024-byte boundary (the swizzle pattern of the tensor
     // layout repeats every 1024 bytes).
@@ -312,7 +316,8 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     const uint32_t ring = smem_u32(smem);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.ring_bytes);
     uint64_t *empty = full + a.ring_stages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + a.ring_stages);
+    uint64_t *recv_bar = empty + a.ring_stages;  // the K-slice partials of my rows (S > 1)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(recv_bar + 1);
     int *armed = const_cast<int *>(abort_flag) + 1;  // last stage armed in each slot
     // (then kMaxSplits ints for the RMSNorm epilogue's "finish this split" flags)
 
@@ -349,6 +354,9 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             mbar_init(smem_u32(&empty[s]), C::kNCW);
             armed[s] = -1;
         }
+        mbar_init(smem_u32(recv_bar), 1);
+        // every slice's block of my rows arrives on recv_bar: expect all of them now
+        if (a.slices > 1) mbar_arrive_expect_tx(smem_u32(recv_bar), static_cast<uint32_t>(kSlots * kSP * 4));
         *abort_flag = 0;
         mbar_fence_init();
         if constexpr (TENSOR) {
@@ -616,6 +624,8 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
 
     // ---- warp partials added in warp order; single-slice CTAs store here ----
     constexpr bool kBf16Out = (COMPUTE == kMmaBf16 || COMPUTE == kFmaBf16);
+    float *stage = red + WK * kSlots * kXP;  // K slices: [owner][row][token], pitch kSP
+    float *recv = stage + kSlots * kSP;      // K slices: [slice][my row][token], pitch kSP
     bool stored = false;
     if (!aborted) {
         for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
@@ -637,7 +647,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                     stored = true;
                 }
             } else {
-                red[slot * kXP + tok] = v;
+                stage[slot * kSP + tok] = v;  // my partial of this row, staged for its owner
             }
         }
     }
@@ -648,39 +658,54 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
 
     if (a.slices > 1) {
         // ---- K slices of the cluster added in slice order ----
-        // Push model: each CTA stores its combined partial P[slot][tok] into the
-        // receive buffer recv[slice][slot - owner*per][tok] of the CTA that owns the
-        // slot (remote stores do not wait); after the second cluster barrier each
-        // owner adds the S slices in slice order from its own shared memory.  recv
-        // sits after the partials in the ring, which every CTA has left once the
-        // first barrier is passed.
+        // Push model with bulk copies: each CTA has staged its combined partial P[slot][tok]
+        // as one contiguous block per owner CTA (owner q holds slots [q * per, (q + 1) * per));
+        // one thread copies block q into recv[slice] of CTA q (a copy between cluster
+        // shared memories, counted in bytes on q's recv_bar, which has expected all S
+        // blocks since the kernel started).  Each owner then adds the S slices of its
+        // rows in slice order.  stage and recv sit after the partials in the ring, which
+        // every CTA has left once the first cluster barrier is passed; its arrival needs
+        // no release ordering (the ring's last reads were consumed before the CTA
+        // barrier above, its copies landed before they were waited on).  The staging
+        // writes reach the copy engine through the proxy fence and the CTA barrier.
         const int per = kSlots / a.slices;
-        float *recv = red + WK * kSlots * kXP;
-        const uint32_t recv_local = smem_u32(recv);
-        // Every CTA has left its ring: its last shared-memory reads were consumed by its
-        // products before the CTA barrier above, and its copies landed before it waited
-        // on them, so the arrival needs no release ordering (a release arrival cost up
-        // to 0.45 us per call at the indexer's tf32 shapes on GB300).  The second barrier
-        // below keeps release / acquire: it publishes the remote stores.
+        const uint32_t block_bytes = static_cast<uint32_t>(per * kSP * 4);
+        fence_proxy_async_smem();
+        __syncthreads();
         cluster_arrive_relaxed();
         cluster_wait();
-        if (!aborted) {
-            for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
-                const int slot = e / kXRows, tok = e - slot * kXRows;
-                if (tok >= a.M || slot >= rows_here) continue;
-                const int q = slot / per;
-                const uint32_t dst = recv_local + static_cast<uint32_t>(((slice * per + slot - q * per) * kXP + tok) * 4);
-                st_shared_cluster_f32(cluster_map_shared(dst, static_cast<uint32_t>(q)), red[slot * kXP + tok]);
-            }
+        if (tid == 0) {
+            const uint32_t recv_local = smem_u32(recv), bar_local = smem_u32(recv_bar), src = smem_u32(stage);
+            for (int q = 0; q < a.slices; ++q)
+                bulk_s2s_cluster(cluster_map_shared(recv_local + slice * block_bytes, static_cast<uint32_t>(q)),
+                                 src + q * block_bytes, block_bytes, cluster_map_shared(bar_local, static_cast<uint32_t>(q)));
         }
-        cluster_sync_all();
-        if (!aborted) {
+        // Every block addressed to this CTA lands before it reads them or exits: the wait
+        // is bounded by time only (not cut short by an earlier timeout of this CTA).
+        {
+            const uint64_t t0 = global_timer_ns();
+            bool got = false;
+            for (uint32_t it = 0;; ++it) {
+                got = mbar_try_wait(smem_u32(recv_bar), 0u);
+                if (__all_sync(0xffffffffu, got)) break;
+                int give_up = 0;
+                if ((it & 7u) == 7u) give_up = (global_timer_ns() - t0 > a.wait_limit_ns) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, give_up, 0)) break;
+            }
+            if (!got && lane == 0) record_timeout(a.err_word, abort_flag);
+        }
+        // First half of the closing cluster barrier: my receive buffer is complete, so
+        // every copy out of a peer's staging block into mine has landed.  The wait comes
+        // last, after the trigger: no CTA leaves while a copy may still read its staging
+        // block.  Relaxed: the data moved by copies that complete on mbarriers.
+        cluster_arrive_relaxed();
+        if (!aborted && *abort_flag == 0) {
             for (int e = tid; e < per * kXRows; e += C::kThreads) {
                 const int tok = e / per, rr = e - tok * per;
                 const int slot = slice * per + rr;
                 if (tok >= a.M || slot >= rows_here) continue;
-                float v = recv[rr * kXP + tok];
-                for (int q = 1; q < a.slices; ++q) v += recv[(q * per + rr) * kXP + tok];
+                float v = recv[rr * kSP + tok];
+                for (int q = 1; q < a.slices; ++q) v += recv[(q * per + rr) * kSP + tok];
                 store_tok<kBf16Out>(out_row<kBf16Out>(a.splits, row0 + slot), tok, v);
                 stored = true;
             }
@@ -692,6 +717,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     if (stored) fence_release_gpu();
     __syncthreads();
     griddep_launch_dependents();
+    if (a.slices > 1) cluster_wait();
 }
 
 }  // namespace hsp
