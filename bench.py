@@ -397,8 +397,8 @@ def time_rmsnorm_variants(hsp, dev, calls, steps, warmup):
         tot, _ = time_graph(g, steps, warmup)
         res[label] = round(tot * 1000.0 / (steps * calls), 4)
         del g
-    res["how"] = ("proj_fused_gemm_rmsnorm (caller workspace) and proj_fused_gemm_rmsnorm_static (built-in "
-                  "array, a 256-byte memset before each kernel) at wq_a++wkv M=8, norm on both splits")
+    res["how"] = ("proj_fused_gemm_rmsnorm (caller workspace) and proj_fused_gemm_rmsnorm_static (the library's "
+                  "built-in array, one kernel per call) at wq_a++wkv M=8, q_norm / kv_norm on both splits")
     del st
     torch.cuda.empty_cache()
     return res
