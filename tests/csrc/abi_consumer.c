@@ -4,6 +4,8 @@
  * the CUDA runtime's C API).
  *
  *   abi_consumer host    queries and argument checks that need no GPU (exit 0 on success)
+ *   abi_consumer reset   calls before and after cudaDeviceReset (this process's context only):
+ *                        the library's per-device caches follow the new context
  *   abi_consumer device  W_cat packed from three weights (proj_pack_weights), then one
  *                        fused and one separate call on small-integer bf16 data,
  *                        checked element by element against a double loop written here
@@ -157,6 +159,88 @@ static int device_checks(void) {
     free(got);
     return failures == 0 ? 0 : 1;
 }
+
+/* One round of calls on freshly allocated buffers: an exact fused call (small integers,
+ * checked against a double loop) and the no-allocation RMSNorm call (status and finite
+ * outputs), then the device error word. */
+static void reset_round(const char *when) {
+    enum { M = 4, K = 192, NS = 2 };
+    const int32_t splits[NS] = {16, 8}, norm_cols[NS] = {16, 8};
+    const int N = 24;
+    uint16_t x[M * K], w[N * K], got[M * 16], gam[16];
+    void *dx = NULL, *dw = NULL, *douts[NS] = {NULL, NULL}, *dg[NS] = {NULL, NULL};
+    const void *gammas[NS];
+    char what[160];
+    int i, m, n, k, s;
+    for (i = 0; i < M * K; ++i) x[i] = bf16_of_int((i * 7) % 3 - 1);
+    for (i = 0; i < N * K; ++i) w[i] = bf16_of_int((i * 5) % 3 - 1);
+    for (i = 0; i < 16; ++i) gam[i] = bf16_of_int(1);
+    if (cudaMalloc(&dx, sizeof x) != cudaSuccess || cudaMalloc(&dw, sizeof w) != cudaSuccess) {
+        ++failures;
+        return;
+    }
+    for (s = 0; s < NS; ++s)
+        if (cudaMalloc(&douts[s], sizeof(uint16_t) * M * splits[s]) != cudaSuccess ||
+            cudaMalloc(&dg[s], sizeof(uint16_t) * 16) != cudaSuccess) {
+            ++failures;
+            return;
+        }
+    cudaMemcpy(dx, x, sizeof x, cudaMemcpyHostToDevice);
+    cudaMemcpy(dw, w, sizeof w, cudaMemcpyHostToDevice);
+    for (s = 0; s < NS; ++s) {
+        cudaMemcpy(dg[s], gam, sizeof(uint16_t) * 16, cudaMemcpyHostToDevice);
+        gammas[s] = dg[s];
+    }
+    snprintf(what, sizeof what, "proj_fused_gemm (%s)", when);
+    check(proj_fused_gemm(dx, dw, splits, NS, douts, M, K, PROJ_BF16, NULL) == PROJ_OK, what);
+    check(cudaDeviceSynchronize() == cudaSuccess, "device synchronise");
+    cudaMemcpy(got, douts[0], sizeof(uint16_t) * M * 16, cudaMemcpyDeviceToHost);
+    for (m = 0; m < M; ++m)
+        for (n = 0; n < 16; ++n) {
+            double want = 0.0;
+            for (k = 0; k < K; ++k) want += double_of_bf16(x[m * K + k]) * double_of_bf16(w[n * K + k]);
+            if (double_of_bf16(got[m * 16 + n]) != want) {
+                snprintf(what, sizeof what, "fused output [%d, %d] exact (%s)", m, n, when);
+                check(0, what);
+                m = M;
+                break;
+            }
+        }
+    for (s = 0; s < NS; ++s) cudaMemset(douts[s], 0xFF, sizeof(uint16_t) * M * splits[s]); /* NaN poison */
+    snprintf(what, sizeof what, "proj_fused_gemm_rmsnorm_static (%s)", when);
+    check(proj_fused_gemm_rmsnorm_static(dx, dw, splits, NS, norm_cols, gammas, 1e-6f, douts, M, K, PROJ_BF16,
+                                         NULL) == PROJ_OK,
+          what);
+    check(cudaDeviceSynchronize() == cudaSuccess, "device synchronise after the static call");
+    cudaMemcpy(got, douts[0], sizeof(uint16_t) * M * 16, cudaMemcpyDeviceToHost);
+    for (i = 0; i < M * 16; ++i)
+        if ((got[i] & 0x7F80) == 0x7F80) {
+            snprintf(what, sizeof what, "static call output %d finite (%s)", i, when);
+            check(0, what);
+            break;
+        }
+    snprintf(what, sizeof what, "no device-side error (%s)", when);
+    check(proj_check_device_error(NULL) == PROJ_OK, what);
+    for (s = 0; s < NS; ++s) {
+        cudaFree(douts[s]);
+        cudaFree(dg[s]);
+    }
+    cudaFree(dx);
+    cudaFree(dw);
+}
+
+/* The library caches per-device facts: the device error word's address, the
+ * no-allocation entry point's array address, kernels' attribute set-up.  A device reset
+ * gives the next context new addresses; every cache is keyed by the context, so calls
+ * after cudaDeviceReset (in this process only) must work as before it. */
+static int reset_checks(void) {
+    reset_round("before the reset");
+    check(cudaDeviceReset() == cudaSuccess, "cudaDeviceReset");
+    reset_round("after the reset");
+    check(cudaDeviceReset() == cudaSuccess, "second cudaDeviceReset");
+    reset_round("after a second reset");
+    return failures == 0 ? 0 : 1;
+}
 #endif
 
 int main(int argc, char **argv) {
@@ -164,6 +248,7 @@ int main(int argc, char **argv) {
     if (strcmp(argv[1], "host") == 0) return host_checks();
 #ifdef ABI_CONSUMER_DEVICE
     if (strcmp(argv[1], "device") == 0) return device_checks();
+    if (strcmp(argv[1], "reset") == 0) return reset_checks();
 #endif
     return 2;
 }

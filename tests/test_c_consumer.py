@@ -53,3 +53,16 @@ def test_plain_c_device_calls_exact(tmp_path):
     exe = _build(tmp_path, device=True)
     r = subprocess.run([exe, "device"], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr + r.stdout
+
+
+@pytest.mark.gpu
+def test_plain_c_calls_survive_a_device_reset(tmp_path):
+    """cudaDeviceReset in a child process (its own context only) between rounds of calls:
+    the library's cached device addresses and kernel set-up follow the new context."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    hsp.lib()
+    exe = _build(tmp_path, device=True)
+    r = subprocess.run([exe, "reset"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr + r.stdout
