@@ -270,3 +270,26 @@ def test_tf32_engines_match_oracle(hsp, name, forced):
             check_close(outs, oracle_outputs(x, w_cat, wl.splits), "tf32", f"{name} engine {forced} M{M}")
     finally:
         hsp.set_options(pdl=True, large_m_path=0)
+
+
+@pytest.mark.parametrize("K,splits,dtype,tf32,forced", [
+    (4100, (40, 24), "fp32", False, 0),     # 16400-byte rows: bulk copies, 8 K slices at M > 8
+    (2056, (17, 47), "fp32", True, 0),      # tf32, 4 K slices
+    (1544, (200, 100), "bf16", False, 1),   # bf16 forced onto the streaming kernel, 2 K slices
+])
+def test_ragged_k_with_k_slices(hsp, K, splits, dtype, tf32, forced):
+    """Rows that are not a whole number of 128-byte units take the bulk-copy layout; with
+    more than 8 tokens they are also cut into K slices whose partials meet through
+    cluster shared memory.  Every M bucket against the oracle, fused and separate."""
+    dt = {"bf16": 0, "fp32": 2 if tf32 else 1}[dtype]
+    hsp.set_options(pdl=True, large_m_path=forced)
+    try:
+        for M in (9, 20, 33, 64):
+            plan = hsp.describe_plan(M, K, sum(splits), dt)
+            assert plan["engine"] == 0 and plan["tensor_copies"] == 0 and plan["slices"] > 1, plan
+            x, ws = W.random_case(K, splits, M, dtype, seed=2100 + M + K)
+            w_cat = torch.cat(ws, 0)
+            outs = _run_both(hsp, x, w_cat, splits, tf32)
+            check_close(outs, oracle_outputs(x, w_cat, splits), mode_of(dtype, tf32), f"ragged K{K} M{M}")
+    finally:
+        hsp.set_options(pdl=True, large_m_path=0)
