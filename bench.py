@@ -421,6 +421,7 @@ def time_config(hsp, wl, M, tf32, dev, calls, steps, warmup, barrier, ws):
            "gpu_launches": steps * calls,
            "achieved_gbs": round(achieved, 1), "frac": round(achieved / peak, 4),
            "engine": ENGINE_NAMES.get(kernel, str(kernel)), "weight_copies": st.copies,
+           "traffic": profiled_traffic(wl.name, M) if not tf32 else None,
            "config": workload_config(wl, M, tf32, ws)}
     del st
     torch.cuda.empty_cache()
