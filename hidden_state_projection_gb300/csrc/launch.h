@@ -23,7 +23,7 @@ inline bool set_up_in_current_context(const std::atomic<uint64_t> &slot) {
 
 struct LaunchReq {
     int compute;     // Compute
-    int bucket;      // 0: (WR, WK) = (1, 8); 1: (2, 4); 2: (4, 2)
+    int bucket;      // 0: (WR, WK) = (1, 8); 1 and 2: (2, 4), fp32 FMA (1, 8)
     int MT;          // token tiles of 8
     int RT;          // 16-row tiles per warp
     int tensor;      // 1: 3-D tensor copies (tmap_w / tmap_x used), 0: 1-D bulk copies

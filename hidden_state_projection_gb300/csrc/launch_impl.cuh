@@ -71,22 +71,54 @@ cudaError_t launch_variant(const LaunchReq &r) {
                     : launch_one<COMPUTE, MT, RT, WR, WK, false, false>(r);
 }
 
+// fp32 FMA above 8 tokens: eight K warps (one 16-byte chunk of every unit each) over
+// 16 to 64 row slots; 64 tokens take at most 32 (8 x 8 register tiles per lane).
+template <int MT>
+cudaError_t launch_fp32_chunk(const LaunchReq &r) {
+    switch (r.RT) {
+        case 1: return launch_variant<kFmaFp32, MT, 1, 1, 8>(r);
+        case 2: return launch_variant<kFmaFp32, MT, 2, 1, 8>(r);
+        case 3:
+            if constexpr (MT < 8) return launch_variant<kFmaFp32, MT, 3, 1, 8>(r);
+            break;
+        case 4:
+            if constexpr (MT < 8) return launch_variant<kFmaFp32, MT, 4, 1, 8>(r);
+            break;
+        default:
+            break;
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
 template <int COMPUTE>
 cudaError_t launch_compute(const LaunchReq &r) {
     const bool rt1 = (r.RT == 1);
+    if constexpr (COMPUTE == kFmaFp32) {
+        if (r.bucket > 0) {
+            if (r.MT == 2) return launch_fp32_chunk<2>(r);
+            if (r.MT == 4) return launch_fp32_chunk<4>(r);
+            if (r.MT == 8) return launch_fp32_chunk<8>(r);
+            return cudaErrorInvalidConfiguration;
+        }
+    }
     switch (r.bucket) {
         case 0:
             if (r.MT != 1) break;
             return rt1 ? launch_variant<COMPUTE, 1, 1, 1, 8>(r) : launch_variant<COMPUTE, 1, 2, 1, 8>(r);
         case 1:
-            if (r.MT == 2)
-                return rt1 ? launch_variant<COMPUTE, 2, 1, 2, 4>(r) : launch_variant<COMPUTE, 2, 2, 2, 4>(r);
-            if (r.MT == 4)
-                return rt1 ? launch_variant<COMPUTE, 4, 1, 2, 4>(r) : launch_variant<COMPUTE, 4, 2, 2, 4>(r);
+            if constexpr (COMPUTE != kFmaFp32) {
+                if (r.MT == 2)
+                    return rt1 ? launch_variant<COMPUTE, 2, 1, 2, 4>(r) : launch_variant<COMPUTE, 2, 2, 2, 4>(r);
+                if (r.MT == 4)
+                    return rt1 ? launch_variant<COMPUTE, 4, 1, 2, 4>(r) : launch_variant<COMPUTE, 4, 2, 2, 4>(r);
+            }
             break;
         case 2:
-            if (r.MT != 8) break;
-            return rt1 ? launch_variant<COMPUTE, 8, 1, 2, 4>(r) : launch_variant<COMPUTE, 8, 2, 2, 4>(r);
+            if constexpr (COMPUTE != kFmaFp32) {
+                if (r.MT == 8)
+                    return rt1 ? launch_variant<COMPUTE, 8, 1, 2, 4>(r) : launch_variant<COMPUTE, 8, 2, 2, 4>(r);
+            }
+            break;
         default:
             break;
     }

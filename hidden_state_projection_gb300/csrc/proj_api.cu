@@ -223,6 +223,7 @@ struct Plan {
     int compute, bucket, MT, RT, WR, WK, S, R, grid_x;
     int units_total, units_per_slice, stage_units, stages_per_slice, ring_stages;
     int tensor;  // 3-D tensor copies (rows a multiple of 128 bytes) or 1-D bulk copies
+    int chunk;   // fp32 FMA above 8 tokens: K warps on 16-byte chunks of every unit
     int pitch, stage_bytes, x_off, ring_bytes, smem;
 };
 
@@ -261,8 +262,14 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     // indexer's 192 rows (28 per CTA) left half the warps without rows (measured on
     // GB300, indexer M = 64: fp32 14.6 -> 14.4 us, tf32 9.9 -> 9.5 us).
     static const int WRs[3] = {1, 2, 2}, WKs[3] = {8, 4, 4};
-    p->WR = WRs[p->bucket];
-    p->WK = WKs[p->bucket];
+    // fp32 FMA above 8 tokens: eight K warps, each on one 16-byte chunk of every unit,
+    // over all row slots of the CTA (balanced for any unit count; measured on GB300,
+    // the FMA loop on a resident stage went from ~53% to ~70% of the FMA pipe at 64
+    // tokens and from ~34% to ~56% at 16)
+    const bool chunk = p->compute == hsp::kFmaFp32 && p->bucket > 0;
+    p->chunk = chunk;
+    p->WR = chunk ? 1 : WRs[p->bucket];
+    p->WK = chunk ? 8 : WKs[p->bucket];
     p->MT = p->bucket == 0 ? 1 : (p->bucket == 2 ? 8 : (M <= 16 ? 2 : 4));
     const int64_t row_bytes = static_cast<int64_t>(K) * esz;
     p->units_total = static_cast<int>((row_bytes + hsp::kUnitBytes - 1) / hsp::kUnitBytes);
@@ -287,6 +294,7 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     // CTA's row slots for the cluster reduction).
     auto slice_units = [&](int S) {
         const int plain = ceil_div(p->units_total, S);
+        if (chunk) return plain;  // every warp has a chunk of every unit already
         const int rounded = ceil_div(plain, p->WK) * p->WK;
         return (S - 1) * rounded < p->units_total ? rounded : plain;
     };
@@ -295,20 +303,25 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
         p->S /= 2;
         p->units_per_slice = slice_units(p->S);
     }
-    const int max_rows = p->WR * 2 * 16;
+    // (the chunk layout: up to four 16-row tiles, two at 64 tokens -- the lane's
+    // register tile is (slots / 4) x 8 there)
+    const int max_rows = chunk ? (p->MT == 8 ? 32 : 64) : p->WR * 2 * 16;
     // rows per CTA: spread over the CTAs that can be resident at once (clusters of
     // S leave some SMs of a GPC idle)
     const int resident = cluster_ctas[p->S] > 0 ? cluster_ctas[p->S] : cluster_ctas[1];
     p->R = ceil_div(n_rows * p->S, resident);
     if (p->R < 1) p->R = 1;
     if (p->R > max_rows) p->R = max_rows;
-    p->RT = p->R > p->WR * 16 ? 2 : 1;
+    p->RT = chunk ? ceil_div(p->R, 16) : (p->R > p->WR * 16 ? 2 : 1);
     const int slots = p->WR * p->RT * 16;
     p->grid_x = ceil_div(n_rows, p->R);
     // partial sums of the warps
     // (rows of 8 * MT + 1 floats, padded against bank conflicts), plus (K slices) the
     // staging and receive blocks of the cluster reduction (rows of 8 * MT + 4 floats)
-    const int red_bytes = p->WK * slots * (8 * p->MT + 1) * 4 + (p->S > 1 ? 2 * slots * (8 * p->MT + 4) * 4 : 0);
+    // (chunk layout: rows of 8 * MT + 32 / row lanes floats, its lanes' tiles write
+    // conflict-free)
+    const int xp = chunk ? 8 * p->MT + (p->MT == 8 ? 8 : 4) : 8 * p->MT + 1;
+    const int red_bytes = p->WK * slots * xp * 4 + (p->S > 1 ? 2 * slots * (8 * p->MT + 4) * 4 : 0);
     const int budget = kSmemLimit - kSmemReserve;
     const int Us = p->units_per_slice;
     p->tensor = (row_bytes % hsp::kUnitBytes) == 0;
@@ -318,6 +331,10 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
         // holding about kStageWeightBytes of weights.  One weight box and one token
         // box per stage, each rounded up to 1024 bytes.
         auto box = [](int rows, int su) { return ceil_div(rows * su * hsp::kUnitBytes, 1024) * 1024; };
+        // The chunk layout keeps every unit's weight rows kSlots lines apart (one box per
+        // unit) and its token rows 8 * MT lines apart (rows past M zero-filled).
+        auto wbox_bytes = [&](int su) { return chunk ? su * slots * hsp::kUnitBytes : box(p->R, su); };
+        auto xbox_bytes = [&](int su) { return chunk ? su * 8 * p->MT * hsp::kUnitBytes : box(M, su); };
         auto choose = [&](int stage_weight_bytes) {
             const int target = std::max(1, stage_weight_bytes / (p->R * hsp::kUnitBytes));
             // the divisor of the slice nearest the target (the larger one on a tie), at
@@ -326,7 +343,7 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
             for (int d = 1; d <= std::max(1, Us / 2); ++d)
                 if (Us % d == 0 && (su == 0 || std::abs(d - target) <= std::abs(su - target))) su = d;
             for (;;) {
-                const int stage = box(p->R, su) + box(M, su);
+                const int stage = wbox_bytes(su) + xbox_bytes(su);
                 const int nst = ceil_div(Us, su);
                 int ring = std::min(std::min(nst, budget / stage), kMaxRingStages);
                 if (ring >= std::min(2, nst) || su == 1) {
@@ -335,7 +352,7 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
                     p->ring_stages = ring;
                     p->pitch = 0;
                     p->stage_bytes = stage;
-                    p->x_off = box(p->R, su);
+                    p->x_off = wbox_bytes(su);
                     return;
                 }
                 int d = su - 1;  // next smaller divisor of the slice
@@ -840,8 +857,11 @@ proj_status launch_rows(const DeviceInfo &dev, const void *x, const void *w, int
         const uint64_t wdims[3] = {ke, static_cast<uint64_t>(n_rows), static_cast<uint64_t>(p.units_total)};
         const uint64_t xdims[3] = {ke, static_cast<uint64_t>(M), static_cast<uint64_t>(p.units_total)};
         const uint64_t strides[2] = {row_bytes, 128u};
-        const uint32_t wbox[3] = {static_cast<uint32_t>(ke), static_cast<uint32_t>(p.R), static_cast<uint32_t>(p.stage_units)};
-        const uint32_t xbox[3] = {static_cast<uint32_t>(ke), static_cast<uint32_t>(M), static_cast<uint32_t>(p.stage_units)};
+        // (chunk layout: one weight box per unit, token boxes 8 * MT rows high)
+        const uint32_t wbox[3] = {static_cast<uint32_t>(ke), static_cast<uint32_t>(p.R),
+                                  static_cast<uint32_t>(p.chunk ? 1 : p.stage_units)};
+        const uint32_t xbox[3] = {static_cast<uint32_t>(ke), static_cast<uint32_t>(p.chunk ? 8 * p.MT : M),
+                                  static_cast<uint32_t>(p.stage_units)};
         proj_status st = encode_map(w, 3, wdims, strides, wbox, dt, &r.tmap_w);
         if (st != PROJ_OK) return st;
         st = encode_map(x, 3, xdims, strides, xbox, dt, &r.tmap_x);

@@ -62,7 +62,9 @@ struct NormArgs {
 //   tensor (rows a multiple of 128 bytes): one 3-D tensor copy per stage for the
 //     weights and one for the tokens, each a box [stage_units][rows][128 bytes]
 //     with the 128-byte swizzle (16-byte chunk c of line L stored at c ^ (L mod 8));
-//     the token box starts x_off bytes (a multiple of 1024) after the weight box;
+//     the token box starts x_off bytes (a multiple of 1024) after the weight box.
+//     (fp32 FMA above 8 tokens: one weight box [R][128 bytes] per unit, unit k at
+//     k * slots lines, and token boxes of 8 * MT rows, the rows past M zero-filled);
 //   bulk (any other K): one 1-D bulk copy per row and stage, rows at `pitch`
 //     (16 mod 128) bytes; the token rows start x_off = R * pitch after the weights.
 struct StreamArgs {

@@ -22,12 +22,15 @@
 //     tail after the last byte).  Otherwise (a ragged last unit) each weight row
 //     and token row of a stage is one 1-D bulk copy of a contiguous segment, rows
 //     padded to a pitch of 16 mod 128 bytes, issued lane-parallel by all nine
-//     warps.  Weight copies of the first ring's worth of stages are issued before
+//     warps.  Weight copies of the first stages (tensor layout: two, one with token
+//     tiles; bulk layout: the first ring's worth) are issued before
 //     griddepcontrol.wait, token copies only after it; a slot is refilled once
 //     every consumer has released it;
 //   * consumer warp (wr, wk) takes every k-unit u (128 bytes of K) of a stage
 //     with u mod WK == wk, for its RT 16-row tiles, and accumulates in registers
-//     (mma.sync bf16 / tf32, or fp32 FMA);
+//     (mma.sync bf16 / tf32, or fp32 FMA); fp32 FMA with more than 8 tokens instead
+//     gives warp wk the 16-byte chunk wk of every unit, for all row slots of the CTA
+//     (equal shares for any unit count, large register tiles);
 //   * the WK warp partials of each output are added in warp order, then (S > 1)
 //     the S CTAs of a cluster, each holding one K slice, add their partials in
 //     slice order through distributed shared memory;
@@ -250,29 +253,57 @@ __device__ __forceinline__ void unit_fma_ksplit(const V &v, int ul, int wr, int 
     }
 }
 
-// FP32 FMA, many tokens (MT >= 2): lane = (row lane rl = lane%4, token lane
-// tl = lane/4); rows wr*RT*16 + rl + 4i (i < 4RT), tokens tl + 8j (j < MT); each
-// output is one sequential fma chain over k.
-template <class C, int RT, int MT, class V>
-__device__ __forceinline__ void unit_fma_outer(const V &v, int ul, int wr, int lane, float (&acc)[4 * RT][MT]) {
-    const int rl = lane & 3, tl = lane >> 2;
-#pragma unroll 2
-    for (int c = 0; c < 8; ++c) {
-        float4 wv[4 * RT], xv[MT];
+// FP32 FMA, more than 8 tokens: warp wk takes the 16-byte chunk wk (4 consecutive k)
+// of EVERY unit, so the eight warps share any unit count equally.  Lane = (row lane
+// rl = lane % LR, token lane tl = lane / LR); it owns rows rl + LR*i (i < RPL) and
+// tokens tl + (32/LR)*j (j < TPL), an RPL x TPL register tile: per unit RPL + TPL
+// 16-byte shared loads feed 4*RPL*TPL FMAs (8 x 8 at 64 tokens: 16 loads per 256 FMAs;
+// measured on GB300 ~70% of the FMA pipe on a resident stage, against ~53% for one
+// unit per warp with 4 x 8 tiles).  Each output of a warp is one sequential fma chain
+// over its chunks in increasing k.
+template <int RPL, int TPL, int LR, class V>
+__device__ __forceinline__ void unit_fma_chunk(const V &v, int ul, int c, int lane, float (&acc)[RPL][TPL]) {
+    constexpr int TS = 32 / LR;
+    const int rl = lane % LR, tl = lane / LR;
+    float4 wv[RPL], xv[TPL];
 #pragma unroll
-        for (int i = 0; i < 4 * RT; ++i) wv[i] = lds128(v.wa(wr * RT * 16 + rl + 4 * i, ul, c));
+    for (int i = 0; i < RPL; ++i) wv[i] = lds128(v.wa(rl + LR * i, ul, c));
 #pragma unroll
-        for (int j = 0; j < MT; ++j) xv[j] = lds128(v.xa(tl + 8 * j, ul, c));
+    for (int j = 0; j < TPL; ++j) xv[j] = lds128(v.xa(tl + TS * j, ul, c));
 #pragma unroll
-        for (int i = 0; i < 4 * RT; ++i)
+    for (int i = 0; i < RPL; ++i)
 #pragma unroll
-            for (int j = 0; j < MT; ++j) {
-                acc[i][j] = fmaf(wv[i].x, xv[j].x, acc[i][j]);
-                acc[i][j] = fmaf(wv[i].y, xv[j].y, acc[i][j]);
-                acc[i][j] = fmaf(wv[i].z, xv[j].z, acc[i][j]);
-                acc[i][j] = fmaf(wv[i].w, xv[j].w, acc[i][j]);
-            }
-    }
+        for (int j = 0; j < TPL; ++j) {
+            acc[i][j] = fmaf(wv[i].x, xv[j].x, acc[i][j]);
+            acc[i][j] = fmaf(wv[i].y, xv[j].y, acc[i][j]);
+            acc[i][j] = fmaf(wv[i].z, xv[j].z, acc[i][j]);
+            acc[i][j] = fmaf(wv[i].w, xv[j].w, acc[i][j]);
+        }
+}
+
+// The same products on the chunk layout's tensor-copy stage: unit rows kSlots (weights)
+// and kXRows (tokens) lines apart, both multiples of 8, so that line rl + LR*i has the
+// swizzle phase rl + LR*i mod 8 = (rl mod 8) + 4*(i odd, LR = 4) in every unit.  w0 / w1
+// (x0 / x1) address the lane's first even / odd row (token) of this unit, chunk swizzled;
+// the other rows follow at compile-time offsets.
+template <int RPL, int TPL, int LR>
+__device__ __forceinline__ void unit_fma_chunk_sw(uint32_t w0, uint32_t w1, uint32_t x0, uint32_t x1,
+                                                  float (&acc)[RPL][TPL]) {
+    constexpr int TS = 32 / LR;
+    float4 wv[RPL], xv[TPL];
+#pragma unroll
+    for (int i = 0; i < RPL; ++i) wv[i] = lds128(((i & 1) ? w1 : w0) + static_cast<uint32_t>(i * LR * kUnitBytes));
+#pragma unroll
+    for (int j = 0; j < TPL; ++j) xv[j] = lds128(((j & 1) ? x1 : x0) + static_cast<uint32_t>(j * TS * kUnitBytes));
+#pragma unroll
+    for (int i = 0; i < RPL; ++i)
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+            acc[i][j] = fmaf(wv[i].x, xv[j].x, acc[i][j]);
+            acc[i][j] = fmaf(wv[i].y, xv[j].y, acc[i][j]);
+            acc[i][j] = fmaf(wv[i].z, xv[j].z, acc[i][j]);
+            acc[i][j] = fmaf(wv[i].w, xv[j].w, acc[i][j]);
+        }
 }
 
 // Zero the bytes [valid, 128) of one k-unit in every loaded row (the tail of K;
@@ -299,10 +330,24 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                       const __grid_constant__ StreamArgs a) {
     using C = StreamCfg<COMPUTE, MT, RT, WR, WK>;
     constexpr int kSlots = C::kSlots, kXRows = C::kXRows;
-    // Row pitch (floats) of the partial-sum and receive buffers: one more than the token
-    // slots, so that a warp reading one token of 32 consecutive rows hits 32 banks (with
-    // a pitch of 8 * MT the combine loop read one bank 8- to 32-fold).
-    constexpr int kXP = kXRows + 1;
+    // fp32 FMA above 8 tokens: one 16-byte chunk of every unit per warp (unit_fma_chunk).
+    // With tensor copies its stage holds each unit's weight rows at a stride of kSlots
+    // lines (one copy per unit) and its token rows at a stride of kXRows lines (token
+    // rows past M zero-filled), so that a lane's swizzle phases do not change from unit
+    // to unit.
+    constexpr bool kChunk = (COMPUTE == kFmaFp32 && MT > 1);
+    static_assert(!kChunk || (WR == 1 && WK == 8), "chunk layout: eight K warps over all row slots");
+    constexpr int kLR = (MT == 8) ? 4 : 8;   // row lanes
+    constexpr int kTS = 32 / kLR;            // token lanes
+    constexpr int kTPL = kXRows / kTS;       // tokens per lane
+    constexpr int kRPL = kSlots / kLR;       // rows per lane
+    // Row pitch (floats) of the partial-sum buffer red[warp][slot][token].  The combine
+    // loop reads one token of 32 consecutive rows per warp instruction (chunk layout: 32
+    // consecutive tokens of one row), so the pitch is one more than the token slots --
+    // 32 banks (a pitch of 8 * MT read one bank 8- to 32-fold).  The chunk layout's lanes
+    // each write a tile of rows rl + kLR*i and tokens tl + kTS*j: with a pitch of
+    // kXRows + kTS (rl * pitch + tl covers 32 banks) those writes are conflict-free too.
+    constexpr int kXP = kChunk ? kXRows + kTS : kXRows + 1;
     // Row pitch of the K-slice reduction's staging and receive blocks: a multiple of
     // four floats, so that each owner's block is a whole number of 16-byte chunks (the
     // unit of a bulk copy between cluster shared memories).
@@ -335,12 +380,28 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     const bool producer = TENSOR && warp == C::kNCW && lane == 0;
 
     const uint64_t w_policy = l2_policy_evict_first();
+    // Tensor layout: weight stages requested before the grid-dependency wait.  The rest of
+    // the first ring goes out after the wait, behind the first stages' token boxes: with
+    // the whole ring requested at entry the DRAM serves every CTA's stages interleaved and
+    // each CTA's first stage lands late (measured on GB300, graphs of back-to-back calls:
+    // two stages instead of the full ring took qk_indexer M = 1 / 8 from 7.96 / 8.34 to
+    // 7.53 / 7.59 us and glm_fused_a M = 1 / 8 from 8.53 / 9.03 to 8.25 / 8.59; with token
+    // tiles one stage did best, fp32 M = 16 6.66 -> 6.49 us, tf32 M = 64 8.67 -> 8.45).
+    constexpr int kPreWaitStages = (MT == 1) ? 2 : 1;
     // every stage's box holds the same bytes (units past the tensor are zero-filled)
-    const uint32_t stage_tx = static_cast<uint32_t>((a.rows_per_cta + a.M) * a.stage_units * kUnitBytes);
+    const uint32_t stage_tx =
+        static_cast<uint32_t>((a.rows_per_cta + (kChunk ? kXRows : a.M)) * a.stage_units * kUnitBytes);
     // ---------------- tensor layout: one producer thread, two boxes per stage ----------------
+    // (chunk layout: one weight box per unit, [R][128 bytes], kSlots lines apart)
     auto tensor_w = [&](int i, int slot) {
-        tma_load_3d_hint(ring + slot * a.stage_bytes, &tmap_w, 0, row0, u_slice0 + i * a.stage_units,
-                         smem_u32(&full[slot]), w_policy);
+        if constexpr (kChunk) {
+            for (int k = 0; k < a.stage_units; ++k)
+                tma_load_3d_hint(ring + slot * a.stage_bytes + static_cast<uint32_t>(k * kSlots * kUnitBytes), &tmap_w,
+                                 0, row0, u_slice0 + i * a.stage_units + k, smem_u32(&full[slot]), w_policy);
+        } else {
+            tma_load_3d_hint(ring + slot * a.stage_bytes, &tmap_w, 0, row0, u_slice0 + i * a.stage_units,
+                             smem_u32(&full[slot]), w_policy);
+        }
     };
     auto tensor_x = [&](int i, int slot) {
         tma_load_3d(ring + slot * a.stage_bytes + a.x_off, &tmap_x, 0, 0, u_slice0 + i * a.stage_units,
@@ -364,7 +425,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             // and before the CTA barrier (they need nothing but the barriers above).
             tma_prefetch_map(&tmap_w);
             tma_prefetch_map(&tmap_x);
-            for (int i = 0; i < npre; ++i) {
+            for (int i = 0; i < min(npre, kPreWaitStages); ++i) {
                 if (i == a.skip_stage) continue;
                 mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx);
                 tensor_w(i, i);
@@ -379,7 +440,7 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     constexpr int kChains = (!kFma && MT == 1) ? 2 : 1;
     float acc_mma[kChains][kFma ? 1 : RT][kFma ? 1 : MT][4];
     float acc_fk[(kFma && MT == 1) ? 4 * RT : 1][8];
-    float acc_fo[(COMPUTE == kFmaFp32 && MT > 1) ? 4 * RT : 1][MT];
+    float acc_fo[kChunk ? kRPL : 1][kChunk ? kTPL : 1];
 #pragma unroll
     for (int i = 0; i < (int)(sizeof(acc_mma) / sizeof(float)); ++i) (&acc_mma[0][0][0][0])[i] = 0.f;
 #pragma unroll
@@ -432,8 +493,15 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     griddep_wait();
     if constexpr (TENSOR) {
         if (producer)
-            for (int i = 0; i < npre; ++i)
-                if (i != a.skip_stage) tensor_x(i, i);
+            for (int i = 0; i < npre; ++i) {
+                if (i == a.skip_stage) continue;
+                if (i >= kPreWaitStages) {  // the rest of the first ring, after its predecessors' tokens
+                    mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx);
+                    tensor_w(i, i);
+                    armed[i] = i;
+                }
+                tensor_x(i, i);
+            }
     } else {
         for (int i = 0; i < npre; ++i) {
             if (i == a.skip_stage) continue;
@@ -500,26 +568,52 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
             v.rmax = rows_here - 1;
             v.tmax = a.M - 1;
             bool zeroed = false;
-            // units of this warp: u = u0 + j with u mod WK == wk, in increasing order
-            for (int u = u0 + ((wk - u0 % WK) % WK + WK) % WK; u < u1; u += WK) {
-                const int ul = u - u0;
-                if constexpr (!TENSOR) {
-                    const int64_t valid = a.row_bytes - static_cast<int64_t>(u) * kUnitBytes;
-                    if (valid < kUnitBytes) {
-                        zero_unit_tail(v, ul, static_cast<uint32_t>(valid), lane);
-                        zeroed = true;
+            if constexpr (kChunk) {
+                // chunk wk of every unit of the stage, in increasing order; a chunk past the
+                // end of the row (bulk layout, ragged last unit) adds nothing and is skipped
+                // (K * 4 is a multiple of 16: a chunk is wholly inside the row or past it)
+                if (has_rows) {
+                    if constexpr (TENSOR) {
+                        // lane offsets of its first even / odd row and token line (chunk wk,
+                        // swizzled); rows past R and tokens past M hold data never stored
+                        const int rl = lane % kLR, tl = lane / kLR;
+                        const uint32_t wb0 = static_cast<uint32_t>(rl * kUnitBytes + ((wk ^ (rl & 7)) << 4));
+                        const uint32_t wb1 = static_cast<uint32_t>(rl * kUnitBytes + ((wk ^ ((rl + kLR) & 7)) << 4));
+                        const uint32_t xb0 = static_cast<uint32_t>(tl * kUnitBytes + ((wk ^ (tl & 7)) << 4));
+                        const uint32_t xb1 = static_cast<uint32_t>(tl * kUnitBytes + ((wk ^ ((tl + kTS) & 7)) << 4));
+#pragma unroll 2
+                        for (int u = u0; u < u1; ++u) {
+                            const uint32_t uw = v.w + static_cast<uint32_t>((u - u0) * kSlots * kUnitBytes);
+                            const uint32_t ux = v.x + static_cast<uint32_t>((u - u0) * kXRows * kUnitBytes);
+                            unit_fma_chunk_sw<kRPL, kTPL, kLR>(uw + wb0, uw + wb1, ux + xb0, ux + xb1, acc_fo);
+                        }
+                    } else {
+#pragma unroll 2
+                        for (int u = u0; u < u1; ++u) {
+                            if (static_cast<int64_t>(u) * kUnitBytes + wk * 16 >= a.row_bytes) continue;
+                            unit_fma_chunk<kRPL, kTPL, kLR>(v, u - u0, wk, lane, acc_fo);
+                        }
                     }
                 }
-                if (!has_rows) continue;
-                if constexpr (COMPUTE == kFmaBf16) {
-                    unit_fma_ksplit<C, RT, 2>(v, ul, wr, lane, a.M, acc_fk);
-                } else if constexpr (COMPUTE == kFmaFp32) {
-                    if constexpr (MT == 1)
-                        unit_fma_ksplit<C, RT, 8>(v, ul, wr, lane, a.M, acc_fk);
-                    else
-                        unit_fma_outer<C, RT, MT>(v, ul, wr, lane, acc_fo);
-                } else {
-                    unit_mma<C, RT, MT, kChains>(v, ul, wr, lane, acc_mma);
+            } else {
+                // units of this warp: u = u0 + j with u mod WK == wk, in increasing order
+                for (int u = u0 + ((wk - u0 % WK) % WK + WK) % WK; u < u1; u += WK) {
+                    const int ul = u - u0;
+                    if constexpr (!TENSOR) {
+                        const int64_t valid = a.row_bytes - static_cast<int64_t>(u) * kUnitBytes;
+                        if (valid < kUnitBytes) {
+                            zero_unit_tail(v, ul, static_cast<uint32_t>(valid), lane);
+                            zeroed = true;
+                        }
+                    }
+                    if (!has_rows) continue;
+                    if constexpr (COMPUTE == kFmaBf16) {
+                        unit_fma_ksplit<C, RT, 2>(v, ul, wr, lane, a.M, acc_fk);
+                    } else if constexpr (COMPUTE == kFmaFp32) {
+                        unit_fma_ksplit<C, RT, 8>(v, ul, wr, lane, a.M, acc_fk);  // MT == 1
+                    } else {
+                        unit_mma<C, RT, MT, kChains>(v, ul, wr, lane, acc_mma);
+                    }
                 }
             }
             if (zeroed) fence_proxy_async_smem();
@@ -588,12 +682,11 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
                         if (c == 0) red[(wk * kSlots + wr * RT * 16 + g + 4 * i) * kXP + t] = v;
                     }
             } else {
-                const int rl = lane & 3, tl = lane >> 2;
+                const int rl = lane % kLR, tl = lane / kLR;
 #pragma unroll
-                for (int i = 0; i < 4 * RT; ++i)
+                for (int i = 0; i < kRPL; ++i)
 #pragma unroll
-                    for (int j = 0; j < MT; ++j)
-                        red[(wk * kSlots + wr * RT * 16 + rl + 4 * i) * kXP + tl + 8 * j] = acc_fo[i][j];
+                    for (int j = 0; j < kTPL; ++j) red[(wk * kSlots + rl + kLR * i) * kXP + tl + kTS * j] = acc_fo[i][j];
             }
         } else {
 #pragma unroll
@@ -629,7 +722,9 @@ __global__ void __launch_bounds__(StreamCfg<COMPUTE, MT, RT, WR, WK>::kThreads, 
     bool stored = false;
     if (!aborted) {
         for (int e = tid; e < kSlots * kXRows; e += C::kThreads) {
-            const int tok = e / kSlots, slot = e - tok * kSlots;
+            // (chunk layout: consecutive threads on consecutive tokens of one row)
+            const int tok = kChunk ? e % kXRows : e / kSlots;
+            const int slot = kChunk ? e / kXRows : e % kSlots;
             if (tok >= a.M || slot >= rows_here) continue;
             float v = red[slot * kXP + tok];
 #pragma unroll

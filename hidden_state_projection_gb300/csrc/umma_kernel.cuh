@@ -10,10 +10,10 @@
 //     default);
 //   * warp 0 lane 0 issues 2-D tensor copies (128-byte swizzle) of the weight box
 //     [tile rows x 128 bytes], L2 evict-first, and the token box [16/32/64 tokens x
-//     128 bytes] of each
-//     k-block into a ring; weight boxes of the first ring's worth of k-blocks go out
-//     before griddepcontrol.wait, token boxes after it (the GLM fused-A order of
-//     TensorRT-LLM PR #20502, glmFusedAGemm commit message);
+//     128 bytes] of each k-block into a ring; the weight boxes of the first two
+//     k-blocks go out before griddepcontrol.wait, token boxes after it (the GLM
+//     fused-A order of TensorRT-LLM PR #20502, glmFusedAGemm commit message), then
+//     the rest of the first ring;
 //   * warp 1 lane 0 issues four tcgen05.mma (M = the tile's weight rows, N = the token tile,
 //     K = 16 bf16 or 8 tf32 each) per k-block into one TMEM accumulator and commits
 //     each stage back to the ring; a final commit marks the accumulator ready;
@@ -47,6 +47,11 @@
 namespace hsp {
 
 constexpr int kUmmaThreads = 128;
+// Weight boxes requested before the grid-dependency wait; the rest of the first ring
+// follows the first token boxes after the wait (measured on GB300, graphs of back-to-back
+// calls: the whole ring at entry 10.22 / 10.31 / 11.38 us at qk_indexer M = 16 / 32 / 64,
+// two boxes 9.84 / 10.09 / 11.22; wq_a++wkv M = 16 8.22 -> 7.90).
+constexpr int kUmmaPreWaitStages = 2;
 
 template <int NT>
 struct UmmaCfg {
@@ -113,11 +118,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         *abort_flag = 0;
         *issued = 0;
         mbar_fence_init();
-        // The producer's first weight boxes go out before the CTA barrier and the TMEM
+        // The producer's first two weight boxes go out before the CTA barrier and the TMEM
         // allocation: they depend on nothing but the barriers initialised just above.
         tma_prefetch_map(&tmap_w);
         tma_prefetch_map(&tmap_x);
-        for (int i = 0; i < min(nkb, a.ring_stages); ++i) {
+        for (int i = 0; i < min(min(nkb, a.ring_stages), kUmmaPreWaitStages); ++i) {
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[i]);
             mbar_expect_tx(fb, w_box);
@@ -160,6 +165,10 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         for (int i = 0; i < npre; ++i) {
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[i]);
+            if (i >= kUmmaPreWaitStages) {  // the rest of the first ring, after the first token boxes
+                mbar_expect_tx(fb, w_box);
+                tma_load_2d_hint(ring + i * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb, w_policy);
+            }
             mbar_arrive_expect_tx(fb, a.x_box_bytes);
             tma_load_2d(ring + i * a.stage_bytes + w_box, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
             *issued = i + 1;
