@@ -14,8 +14,9 @@
 //   * rows go in blocks of kGemvRows; a block's chunks are loaded straight into
 //     registers (read-only path, no L1 allocation, L2 evict-first), two blocks in
 //     flight: the first two before griddepcontrol.wait, at kernel entry;
-//   * the tokens X[M, K] arrive after the grid-dependency wait as one 1-D bulk copy
-//     into shared memory (contiguous rows; thread t reads its own chunks, conflict free);
+//   * the tokens X[M, K] arrive after the grid-dependency wait as eight 1-D bulk copies
+//     into shared memory, issued from a different piece in each CTA (contiguous rows;
+//     thread t reads its own chunks, conflict free);
 //   * each thread keeps one fp32 FMA chain per (row, token): its chunks in increasing
 //     order, the 4 floats of a chunk in k order; the 32 lanes of a warp are then added
 //     by a fixed butterfly and the 16 warps in warp order.  The order depends on K only,
@@ -126,7 +127,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_
     if (tid == 0 && x_issued) {
         const uint32_t bytes = static_cast<uint32_t>(Mh) * static_cast<uint32_t>(a.row_bytes);
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_copy_g2s(smem_u32(xs), a.x + static_cast<int64_t>(tok0) * a.row_bytes, bytes, bar);
+        // Every CTA reads the same token bytes at about the same time: eight pieces, each
+        // CTA starting at a different one, spread the requests over the L2 slices
+        // (measured on GB300: indexer M = 4 5.32 -> 5.15 us, router M = 4 5.01 -> 4.90).
+        constexpr uint32_t kPieces = 8;
+        const uint32_t piece = (bytes + kPieces * 16 - 1) / (kPieces * 16) * 16;
+        for (uint32_t q = 0; q < kPieces; ++q) {
+            const uint32_t off = ((q + blockIdx.x) % kPieces) * piece;
+            if (off >= bytes) continue;
+            bulk_copy_g2s(smem_u32(xs) + off, a.x + static_cast<int64_t>(tok0) * a.row_bytes + off,
+                          min(piece, bytes - off), bar);
+        }
     }
     if (warp == kGemvWarps - 1 && a.prefetch.count > 0)
         prefetch_ranges_l2(a.prefetch, blockIdx.x, gridDim.x, lane);
