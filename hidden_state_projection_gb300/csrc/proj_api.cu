@@ -279,15 +279,21 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
     p->S = 1;
     if (p->bucket > 0 && esz == 4 && p->units_total >= 128) {
         // fp32 rows of 16 KB and more with many tokens: every row tile re-reads its K
-        // slice of all token rows, so slices must be short -- sixteen of them
-        p->S = 16;
+        // slice of all token rows, so slices must be short -- sixteen of them (tf32 at
+        // 9-32 tokens: eight, its mma.sync products leave the reduction the larger part;
+        // measured on GB300, indexer M = 9 / 16 / 32 5.47 / 5.59 / 7.00 -> 5.34 / 5.45 /
+        // 6.65 us, router M = 16 6.30 -> 6.02; fp32 FMA stays faster with sixteen)
+        p->S = (dt == PROJ_TF32 && p->bucket == 1) ? 8 : 16;
     } else if (p->bucket > 0) {
         if (per_warp >= 16) p->S = 4;
         else if (per_warp >= 4) p->S = 2;
     } else if (esz == 4 && per_warp >= 16) {
         // fp32 rows are twice as long: few rows per CTA would leave most SMs idle and
-        // long per-warp chains; four K slices per row instead (fixed per K and dtype)
-        p->S = 4;
+        // long per-warp chains; eight K slices per row instead (fixed per K and dtype;
+        // measured on GB300 against four: tf32 indexer M = 1 / 4 / 8 5.17 / 5.18 / 5.41 ->
+        // 4.89 / 4.89 / 5.11 us, fp32 indexer M = 7 / 8 6.84 / 6.88 -> 6.01 / 6.03; two
+        // and sixteen were slower)
+        p->S = 8;
     }
     // Units per slice: a multiple of WK when that leaves no slice empty (balanced
     // warps), else the plain share.  S stays a power of two (it must divide the
