@@ -76,6 +76,26 @@ def test_edge_shapes(hsp, dtype, K, splits, M):
         check_close(outs, oracle_outputs(x, w_cat, splits), mode_of(dtype, tf32), f"K{K}")
 
 
+@pytest.mark.parametrize("K,splits,M,row_tiles,token_tiles,slices", [
+    (4096, (300, 100), 12, 4, 2, 16),   # 58 rows per CTA: four 16-row tiles, 4 x 2 lane tiles
+    (4096, (300, 100), 24, 4, 4, 16),   # four tiles, 4 x 8 lane tiles
+    (4096, (200, 100), 20, 3, 4, 16),   # 43 rows per CTA: three tiles
+    (4096, (300, 100), 40, 2, 8, 16),   # 33-64 tokens: at most two tiles (8 x 8), two waves of CTAs
+    (2048, (60, 40), 10, 1, 2, 2),      # one tile, two K slices
+])
+def test_fp32_chunk_layout_tiles(hsp, K, splits, M, row_tiles, token_tiles, slices):
+    """fp32 above 8 tokens: eight K warps, each on one 16-byte chunk of every unit, over
+    one to four 16-row tiles (two at most from 33 tokens).  Every instance the planner can
+    pick, against the oracle, fused and separate."""
+    plan = hsp.describe_plan(M, K, sum(splits), 1)
+    assert (plan["engine"], plan["k_warps"], plan["row_warps"]) == (0, 8, 1), plan
+    assert (plan["row_tiles"], plan["token_tiles"], plan["slices"]) == (row_tiles, token_tiles, slices), plan
+    x, ws = W.random_case(K, splits, M, "fp32", seed=3300 + K + M)
+    w_cat = torch.cat(ws, 0)
+    outs = _run_both(hsp, x, w_cat, splits)
+    check_close(outs, oracle_outputs(x, w_cat, splits), "fp32", f"chunk K{K} M{M} RT{row_tiles}")
+
+
 @pytest.mark.parametrize("dtype,tf32", [("bf16", False), ("fp32", False), ("fp32", True)])
 def test_every_token_count(hsp, dtype, tf32):
     K, splits = 1536, (200, 56)
