@@ -19,9 +19,10 @@
 //     thread t reads its own chunks, conflict free);
 //   * each thread keeps one fp32 FMA chain per (row, token): its chunks in increasing
 //     order, the 4 floats of a chunk in k order; the 32 lanes of a warp are then added
-//     by a fixed butterfly and the 16 warps in warp order.  The order depends on K only,
-//     so fused and per-projection launches, repeats and graph replays give identical
-//     bits; the chains are at most 16 terms long, well inside the fp32 tolerance;
+//     by a fixed transposing reduction and the 16 warps in warp order.  The order
+//     depends on K only, so fused and per-projection launches, repeats and graph
+//     replays give identical bits; the chains are at most 16 terms long, well inside
+//     the fp32 tolerance;
 //   * every storing thread fences, the CTA synchronises, and only then is the dependent
 //     launch triggered (the trigger follows the stores).
 //
@@ -198,21 +199,37 @@ __global__ void __launch_bounds__(kGemvThreads, 1) hsp_gemv_kernel(const __grid_
             }
         }
         if (b + 2 < nblk) load_block(buf, b + 2);
-        // lanes of a warp by a fixed butterfly, then warps in order
+        // Lanes of a warp by a fixed transposing reduction over all 16 (row, token) slots
+        // (token slots past the group's tokens hold zeros): at offsets 16, 8, 4 and 2 each
+        // lane keeps half of its values and adds the partner's copy of that half, so lane
+        // l ends with slot (l >> 1) & 15 summed over 16 lanes; offset 1 adds the last pair.
+        // 16 shuffles per lane for any token count (a butterfly per slot took 5 per slot:
+        // 40 at four tokens).  Then the warps in order.
+        static_assert(kGemvRows * 8 == 16, "the transposing reduction covers 16 slots");
+        float v[16];
 #pragma unroll
         for (int r = 0; r < kGemvRows; ++r)
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                if (t < Mh) {
-                    float v = acc[r][t];
-                    v += __shfl_xor_sync(0xffffffffu, v, 16);
-                    v += __shfl_xor_sync(0xffffffffu, v, 8);
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    if (lane == 0) part[warp][r][t] = v;
+            for (int t = 0; t < 8; ++t) v[r * 8 + t] = acc[r][t];
+        int n = 16;
+#pragma unroll
+        for (int o = 16; o >= 2; o >>= 1) {
+            const bool upper = (lane & o) != 0;  // keep the upper half, send the lower
+            n >>= 1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < n) {
+                    const float keep = upper ? v[i + n] : v[i];
+                    const float send = upper ? v[i] : v[i + n];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                 }
             }
+        }
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        {
+            const int slot = (lane >> 1) & 15, r = slot >> 3, t = slot & 7;
+            if ((lane & 1) == 0 && t < Mh) part[warp][r][t] = v[0];
+        }
         __syncthreads();
         if (abort_flag == 0 && tid < kGemvRows * Mh) {
             const int r = tid / Mh, t = tid - r * Mh;
