@@ -19,11 +19,13 @@
 //     reads sit in eight different bank groups.  The copy engine accepts about one
 //     copy per 55 cycles per SM, so one large box per stage replaces the R + M
 //     row copies of the other layout and leaves the stages short (small compute
-//     tail after the last byte).  Otherwise (a ragged last unit) each weight row
-//     and token row of a stage is one 1-D bulk copy of a contiguous segment, rows
-//     padded to a pitch of 16 mod 128 bytes, issued lane-parallel by all nine
-//     warps.  Weight copies of the first stages (tensor layout: two, one with token
-//     tiles; bulk layout: the first ring's worth) are issued before
+//     tail after the last byte).  (fp32 FMA above 8 tokens: one weight box per
+//     unit, [R rows][128 bytes], so that every unit starts on the same swizzle
+//     phase, and token boxes 8 * MT rows high.)  Otherwise (a ragged last unit)
+//     each weight row and token row of a stage is one 1-D bulk copy of a contiguous
+//     segment, rows padded to a pitch of 16 mod 128 bytes, issued lane-parallel by
+//     all nine warps.  Weight copies of the first stages (tensor layout: two, one
+//     with token tiles; bulk layout: the first ring's worth) are issued before
 //     griddepcontrol.wait, token copies only after it; a slot is refilled once
 //     every consumer has released it;
 //   * consumer warp (wr, wk) takes every k-unit u (128 bytes of K) of a stage
