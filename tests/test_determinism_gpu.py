@@ -99,6 +99,26 @@ def test_graph_replay_matches_eager(hsp, name, M, tf32, separate):
     hsp.check_device_error()
 
 
+@pytest.mark.parametrize("reg_path,M", [(0, 4), (2, 7), (2, 17)])
+def test_register_gemv_token_bits_do_not_depend_on_the_group(hsp, reg_path, M):
+    """The register GEMV adds each (row, token) over all of K in one CTA, by a reduction
+    tree that does not depend on how many tokens the CTA holds: every token of a call
+    with M tokens (reg_path 2: in groups of up to 6 at K = 7168) has the bits of a call
+    with that token alone."""
+    wl, x, w = _inputs("indexer_fp32", M, 2)
+    hsp.set_options(pdl=True, reg_path=reg_path)
+    try:
+        assert hsp.describe_plan(M, wl.K, wl.n_total, 1)["engine"] == 3
+        full = hsp.fused_gemm(x, w, wl.splits)
+        for t in range(M):
+            one = hsp.fused_gemm(x[t:t + 1].contiguous(), w, wl.splits)
+            for a, b in zip(full, one):
+                assert torch.equal(a[t:t + 1], b), (M, t)
+        hsp.check_device_error()
+    finally:
+        hsp.set_options(pdl=True, reg_path=0)
+
+
 def test_launch_counting(hsp):
     wl, x, w = _inputs("qk_indexer", 8, 0)
     n0 = hsp.launch_count()
