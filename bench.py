@@ -369,8 +369,9 @@ def cpu_baseline(wl, M, budget_s=12.0):
 
 def time_rmsnorm_variants(hsp, dev, calls, steps, warmup):
     """µs per call of the RMSNorm-epilogue call at wq_a++wkv M = 8 (q_norm / kv_norm on
-    both splits), with a caller workspace and with the library's fixed array (whose
-    per-call counter clear is a memset between the kernels), same rotation as above."""
+    both splits), with a caller workspace and with the library's fixed array (one kernel
+    per call either way: every call leaves the arrival counters at zero), same rotation
+    as above."""
     wl, M, cols = W.WORKLOADS["wq_a_wkv"], 8, (1280, 512)
     st = Setup(wl, M, dev)
     g0 = torch.Generator().manual_seed(3)

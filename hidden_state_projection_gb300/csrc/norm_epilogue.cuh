@@ -120,7 +120,7 @@ __device__ __noinline__ bool norm_epilogue(const StreamArgs &a, float *red, int 
                          ((reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(gamma)) & 15u) == 0;
         const int c8 = c >> 3, items = vec ? c8 * M : 0;
         // This thread's first kNormItems items are requested before the sums of squares
-        // are added, so their loads overlap the partial-sum loads below.
+        // are added, so their loads overlap the staging and the sums below.
         float4 va[kNormItems], vb[kNormItems];
         uint4 gv[kNormItems];
         auto load_items = [&](int base) {
@@ -135,10 +135,27 @@ __device__ __noinline__ bool norm_epilogue(const StreamArgs &a, float *red, int 
                 }
             }
         };
+        // The per-CTA sums of squares head the chain to the scales: their loads go out
+        // first, then this thread's first items, which overlap the staging and the sums
+        // (items first put ~100 KB of value loads ahead of them).
+        constexpr int kPartBatch = 4;
+        float pv[kPartBatch];
+        if (staged) {
+#pragma unroll
+            for (int j = 0; j < kPartBatch; ++j) {
+                const int e = tid + j * nthreads;
+                pv[j] = e < np ? __ldcg(&parts[e]) : 0.f;
+            }
+        }
         load_items(tid);
         __syncthreads();
         if (staged) {
-            for (int e = tid; e < np; e += nthreads) scratch[e] = __ldcg(&parts[e]);
+#pragma unroll
+            for (int j = 0; j < kPartBatch; ++j) {
+                const int e = tid + j * nthreads;
+                if (e < np) scratch[e] = pv[j];
+            }
+            for (int e = tid + kPartBatch * nthreads; e < np; e += nthreads) scratch[e] = __ldcg(&parts[e]);
             __syncthreads();
         }
         if (staged) {
