@@ -50,13 +50,15 @@ def dist_env():
 
 # The device-code files of each kernel family: its header, its instances and the
 # headers it includes.  A profile's DRAM counters stay valid while these are unchanged.
+# a kernel's device sources: its header, its instance files and the headers they include
 KERNEL_FILES = {
-    "reg": ["reg_kernel.cuh", "kernels_reg.cu"],
+    "reg": ["reg_kernel.cuh", "kernels_reg.cu", "norm_epilogue.cuh"],
     "gemv": ["gemv_kernel.cuh", "kernels_gemv.cu"],
-    "stream": ["stream_kernel.cuh", "launch_impl.cuh", "kernels_bf16.cu", "kernels_tf32.cu", "kernels_fp32.cu"],
+    "stream": ["stream_kernel.cuh", "launch_impl.cuh", "kernels_bf16.cu", "kernels_tf32.cu", "kernels_fp32.cu",
+               "norm_epilogue.cuh"],
     "umma": ["umma_kernel.cuh", "kernels_umma.cu"],
 }
-SHARED_FILES = ["ptx.cuh", "scatter.cuh", "norm_epilogue.cuh", "prefetch.cuh", "stream_args.h"]
+SHARED_FILES = ["ptx.cuh", "scatter.cuh", "prefetch.cuh", "stream_args.h"]
 
 
 def strip_comments(src: str) -> str:
