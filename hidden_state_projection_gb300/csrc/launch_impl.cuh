@@ -72,15 +72,13 @@ cudaError_t launch_variant(const LaunchReq &r) {
 }
 
 // fp32 FMA above 8 tokens: eight K warps (one 16-byte chunk of every unit each) over
-// 16 to 64 row slots; 64 tokens take at most 32 (8 x 8 register tiles per lane).
+// 16 to 64 row slots; 33-64 tokens take at most 48 (12 x 8 register tiles per lane).
 template <int MT>
 cudaError_t launch_fp32_chunk(const LaunchReq &r) {
     switch (r.RT) {
         case 1: return launch_variant<kFmaFp32, MT, 1, 1, 8>(r);
         case 2: return launch_variant<kFmaFp32, MT, 2, 1, 8>(r);
-        case 3:
-            if constexpr (MT < 8) return launch_variant<kFmaFp32, MT, 3, 1, 8>(r);
-            break;
+        case 3: return launch_variant<kFmaFp32, MT, 3, 1, 8>(r);
         case 4:
             if constexpr (MT < 8) return launch_variant<kFmaFp32, MT, 4, 1, 8>(r);
             break;

@@ -309,9 +309,11 @@ void make_plan(int M, int K, int n_rows, proj_dtype dt, const int *cluster_ctas,
         p->S /= 2;
         p->units_per_slice = slice_units(p->S);
     }
-    // (the chunk layout: up to four 16-row tiles, two at 64 tokens -- the lane's
-    // register tile is (slots / 4) x 8 there)
-    const int max_rows = chunk ? (p->MT == 8 ? 32 : 64) : p->WR * 2 * 16;
+    // (the chunk layout: up to four 16-row tiles, three at 33-64 tokens -- the lane's
+    // register tile is (slots / 4) x 8 there, 12 x 8 at three tiles; measured on GB300,
+    // router 256 x 6144 at M = 33 / 48 / 64: 18.95 / 19.13 / 19.61 us with two tiles (its
+    // CTAs in two waves) -> 13.82 / 13.96 / 14.40 with three; the indexer keeps two)
+    const int max_rows = chunk ? (p->MT == 8 ? 48 : 64) : p->WR * 2 * 16;
     // rows per CTA: spread over the CTAs that can be resident at once (clusters of
     // S leave some SMs of a GPC idle)
     const int resident = cluster_ctas[p->S] > 0 ? cluster_ctas[p->S] : cluster_ctas[1];
@@ -538,7 +540,7 @@ bool use_umma(int M, proj_dtype dt) {
 
 struct UPlan {
     proj_plan_info info;
-    int compute, NT, S, TR, kb_total, kb_per_slice, tiles, ring, stage_bytes, x_box, smem;
+    int compute, NT, S, TR, kb_total, kb_per_slice, tiles, ring, stage_bytes, x_box, smem, G;
 };
 
 // K slices and k-blocks per slice depend on (K, dtype) only (the summation order).  The
@@ -574,8 +576,17 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_cta
     const bool few = ceil_div(n_rows, 128) * p->S * 4 <= pair_ctas[1];
     p->TR = ((p->NT == 64 || few) && ceil_div(n_rows, 64) * p->S <= wave) ? 64 : 128;
     p->tiles = ceil_div(n_rows, p->TR);
-    p->x_box = p->NT * 128;
-    p->stage_bytes = p->TR * 128 + p->x_box;
+    // Two k-blocks per stage (one 3-D box of weights, 256 contiguous bytes of each row,
+    // and one of tokens) for the 64-row tiles at 64 tokens: measured on GB300, qk_indexer
+    // M = 64 10.95 -> 10.37 us, wq_a++wkv M = 64 8.75 -> 8.21 (at 16-32 tokens with
+    // 128-row tiles it was mixed, qk_indexer M = 32 10.08 -> 10.34).  Only where rows are
+    // whole k-blocks and the slices' and the total k-block counts are even: no stage then
+    // reaches past its slice or adds a zero-filled k-block, so the products and their
+    // order, hence every output bit, are those of one k-block per stage.
+    p->G = (p->TR == 64 && p->NT == 64 && row_bytes % 128 == 0 && p->kb_total % 2 == 0 && p->kb_per_slice % 2 == 0)
+               ? 2 : 1;
+    p->x_box = p->G * p->NT * 128;
+    p->stage_bytes = p->G * p->TR * 128 + p->x_box;
     // receive buffer of the cluster reduction (dedicated); the staging buffer aliases
     // the ring.  Two CTAs per SM: ring + receive buffer within ~110 KB.
     const int red_bytes = p->TR * (p->NT + 4) * 4;
@@ -585,9 +596,11 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_cta
     // GB300, qk_indexer M = 33 / 48 / 64 10.99 / 10.98 / 11.18 -> 10.69 / 10.70 / 10.92 us,
     // wq_a++wkv M = 64 8.93 -> 8.71; three stages gained less).  The ring depth does not
     // change any output bit.
-    if (p->TR == 64 && p->NT == 64 && ring > 4) ring = 4;
+    // (four one-k-block stages, or two of two k-blocks: 64 KB in flight either way)
+    if (p->TR == 64 && p->NT == 64 && ring > 4 / p->G) ring = 4 / p->G;
     if (ring < 2) ring = 2;
-    if (ring > p->kb_per_slice) ring = p->kb_per_slice < 2 ? 2 : p->kb_per_slice;
+    const int stages = p->kb_per_slice / p->G;
+    if (ring > stages) ring = stages < 2 ? 2 : stages;
     while (p->S > 1 && ring * p->stage_bytes < red_bytes) ++ring;
     p->ring = ring;
     p->smem = 1024 + ring * p->stage_bytes + recv_bytes + (2 * ring + 2) * 8 + 16 + 64;
@@ -604,8 +617,8 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_cta
     i.ring_stages = p->ring;
     i.stage_bytes = p->stage_bytes;
     i.smem_bytes = p->smem;
-    i.k_per_stage = 128 / elem_size(dt);
-    i.stages_total = p->kb_per_slice;
+    i.k_per_stage = p->G * 128 / elem_size(dt);
+    i.stages_total = p->kb_per_slice / p->G;
     i.threads = hsp::kUmmaThreadsHost;
     i.units_per_slice = p->kb_per_slice;
     i.engine = 1;
@@ -618,12 +631,28 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
     make_umma_plan(M, K, n_rows, dt, dev.pair_ctas, &p);
     hsp::UmmaLaunchReq r{};
     const uint32_t boxk = 128u / static_cast<uint32_t>(elem_size(dt));
-    proj_status st = encode_map(w, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), boxk,
-                                static_cast<uint32_t>(p.TR), dt, &r.tmap_w);
-    if (st != PROJ_OK) return st;
-    st = encode_map(x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), boxk, static_cast<uint32_t>(p.NT), dt,
-                    &r.tmap_x);
-    if (st != PROJ_OK) return st;
+    proj_status st;
+    if (p.G == 2) {
+        // [k-blocks][rows][128 bytes] (row stride row_bytes, k-block stride 128 bytes),
+        // boxes [2][tile rows or token tile][128 bytes]
+        const uint64_t rb = static_cast<uint64_t>(K) * elem_size(dt);
+        const uint64_t strides[2] = {rb, 128u};
+        const uint64_t wdims[3] = {boxk, static_cast<uint64_t>(n_rows), static_cast<uint64_t>(p.kb_total)};
+        const uint64_t xdims[3] = {boxk, static_cast<uint64_t>(M), static_cast<uint64_t>(p.kb_total)};
+        const uint32_t wbox[3] = {boxk, static_cast<uint32_t>(p.TR), 2u};
+        const uint32_t xbox[3] = {boxk, static_cast<uint32_t>(p.NT), 2u};
+        st = encode_map(w, 3, wdims, strides, wbox, dt, &r.tmap_w);
+        if (st != PROJ_OK) return st;
+        st = encode_map(x, 3, xdims, strides, xbox, dt, &r.tmap_x);
+        if (st != PROJ_OK) return st;
+    } else {
+        st = encode_map(w, static_cast<uint64_t>(K), static_cast<uint64_t>(n_rows), boxk, static_cast<uint32_t>(p.TR), dt,
+                        &r.tmap_w);
+        if (st != PROJ_OK) return st;
+        st = encode_map(x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), boxk, static_cast<uint32_t>(p.NT), dt,
+                        &r.tmap_x);
+        if (st != PROJ_OK) return st;
+    }
     r.compute = p.compute;
     r.NT = p.NT;
     r.grid = dim3(static_cast<unsigned>(p.tiles), static_cast<unsigned>(p.S), 1);
@@ -641,6 +670,7 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
     a.ring_stages = p.ring;
     a.stage_bytes = static_cast<uint32_t>(p.stage_bytes);
     a.x_box_bytes = static_cast<uint32_t>(p.x_box);
+    a.kb_per_stage = p.G;
     a.prefetch_l2 = g_opt_l2_prefetch.load();
     a.trigger_early = g_opt_trigger_early.load();
     a.skip_stage = g_opt_skip_stage_plus1.load() - 1;

@@ -105,12 +105,12 @@ struct UmmaArgs {
     int32_t kb_per_slice;      // k-blocks of one K slice
     int32_t slices;            // S (cluster size along grid.y)
     int32_t ring_stages;
-    uint32_t stage_bytes;      // 16384 (weight box) + x_box_bytes, a multiple of 1024
-    uint32_t x_box_bytes;      // token rows (16, 32 or 64) * 128
+    uint32_t stage_bytes;      // weight boxes (tile rows * 128 per k-block) + x_box_bytes, a multiple of 1024
+    uint32_t x_box_bytes;      // token rows (16, 32 or 64) * 128 per k-block of the stage
     int32_t prefetch_l2;       // 1: bulk-prefetch the CTA's weight segments into L2 first
     int32_t skip_stage;        // test hook: this k-block of every slice is never loaded (-1: off)
     int32_t trigger_early;     // option: trigger dependents at kernel start (default: after the stores)
-    int32_t pad_;
+    int32_t kb_per_stage;      // k-blocks per ring stage: 1 (2-D boxes) or 2 (one 3-D box each of weights and tokens)
     uint64_t wait_limit_ns;
     int *err_word;
     SplitTable splits;

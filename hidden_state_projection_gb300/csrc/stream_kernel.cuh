@@ -260,6 +260,7 @@ __device__ __forceinline__ void unit_fma_ksplit(const V &v, int ul, int wr, int 
 // rl = lane % LR, token lane tl = lane / LR); it owns rows rl + LR*i (i < RPL) and
 // tokens tl + (32/LR)*j (j < TPL), an RPL x TPL register tile: per unit RPL + TPL
 // 16-byte shared loads feed 4*RPL*TPL FMAs (8 x 8 at 64 tokens: 16 loads per 256 FMAs;
+// 12 x 8 with three row tiles;
 // measured on GB300 ~70% of the FMA pipe on a resident stage, against ~53% for one
 // unit per warp with 4 x 8 tiles).  Each output of a warp is one sequential fma chain
 // over its chunks in increasing k.

@@ -8,15 +8,17 @@
 //   * with the l2_prefetch option, warps 2-3 first bulk-prefetch the CTA's weight
 //     segments (one contiguous run per row) into L2 (measured slower on GB300: off by
 //     default);
-//   * warp 0 lane 0 issues 2-D tensor copies (128-byte swizzle) of the weight box
+//   * warp 0 lane 0 issues tensor copies (128-byte swizzle) of the weight box
 //     [tile rows x 128 bytes], L2 evict-first, and the token box [16/32/64 tokens x
-//     128 bytes] of each k-block into a ring; the weight boxes of the first two
-//     k-blocks go out before griddepcontrol.wait, token boxes after it (the GLM
-//     fused-A order of TensorRT-LLM PR #20502, glmFusedAGemm commit message), then
-//     the rest of the first ring;
+//     128 bytes] of each ring stage: one k-block per stage (2-D boxes), or two (3-D
+//     boxes [2][rows][128 bytes], 256 contiguous bytes of every weight row per copy);
+//     the weight boxes of the first two stages go out before griddepcontrol.wait,
+//     token boxes after it (the GLM fused-A order of TensorRT-LLM PR #20502,
+//     glmFusedAGemm commit message), then the rest of the first ring;
 //   * warp 1 lane 0 issues four tcgen05.mma (M = the tile's weight rows, N = the token tile,
-//     K = 16 bf16 or 8 tf32 each) per k-block into one TMEM accumulator and commits
-//     each stage back to the ring; a final commit marks the accumulator ready;
+//     K = 16 bf16 or 8 tf32 each) per k-block, k-blocks in order, into one TMEM
+//     accumulator and commits each stage back to the ring; a final commit marks the
+//     accumulator ready;
 //   * all four warps read the accumulator (warp w reads TMEM lanes 32w..32w+31: one
 //     weight row per thread, or per lane < 16 for a 64-row tile), then either store
 //     (S = 1) or stage the partials per
@@ -81,7 +83,9 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     // A stage is the weight box [tile rows][128 bytes] followed by the token box, so the
     // tile height (64 or 128 weight rows, the MMA's M) is what the token box leaves.
     const uint32_t w_box = a.stage_bytes - a.x_box_bytes;
-    const int TR = static_cast<int>(w_box >> 7);
+    const int G = a.kb_per_stage == 2 ? 2 : 1;  // k-blocks per stage
+    const int TR = static_cast<int>((w_box / G) >> 7);
+    const uint32_t x_kb = a.x_box_bytes / G;    // one k-block of the token box
     const uint32_t red_bytes = static_cast<uint32_t>(TR) * kPitch * 4u;  // one partial per row of the tile
     const uint32_t ring_bytes = a.ring_stages * a.stage_bytes;
     float *recv = reinterpret_cast<float *>(smem + ring_bytes);  // K-slice partials of my rows (S > 1)
@@ -105,6 +109,17 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
     // neighbouring kernels share stay in L2 (measured on GB300 at qk_indexer M = 64:
     // 11.98 -> 11.23 us per call; the first token boxes otherwise came from DRAM).
     const uint64_t w_policy = l2_policy_evict_first();
+    // Stages of this slice (with two k-blocks per stage the planner makes every slice's
+    // k-block count even, so no stage reaches past its slice).
+    const int nst = (nkb + G - 1) / G;
+    auto load_w = [&](int i, uint32_t dst, uint32_t fb) {
+        if (G == 1) tma_load_2d_hint(dst, &tmap_w, (kb0 + i) * kBoxK, row0, fb, w_policy);
+        else tma_load_3d_hint(dst, &tmap_w, 0, row0, kb0 + 2 * i, fb, w_policy);
+    };
+    auto load_x = [&](int i, uint32_t dst, uint32_t fb) {
+        if (G == 1) tma_load_2d(dst, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
+        else tma_load_3d(dst, &tmap_x, 0, 0, kb0 + 2 * i, fb);
+    };
 
     if (tid == 0) {
         for (int s = 0; s < a.ring_stages; ++s) {
@@ -122,11 +137,11 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         // allocation: they depend on nothing but the barriers initialised just above.
         tma_prefetch_map(&tmap_w);
         tma_prefetch_map(&tmap_x);
-        for (int i = 0; i < min(min(nkb, a.ring_stages), kUmmaPreWaitStages); ++i) {
+        for (int i = 0; i < min(min(nst, a.ring_stages), kUmmaPreWaitStages); ++i) {
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[i]);
             mbar_expect_tx(fb, w_box);
-            tma_load_2d_hint(ring + i * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb, w_policy);
+            load_w(i, ring + i * a.stage_bytes, fb);
         }
     }
     if (warp == 2) {
@@ -160,20 +175,20 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // ---------------- copy producer (its first weight boxes are already out) ----------------
-        const int npre = min(nkb, a.ring_stages);
+        const int npre = min(nst, a.ring_stages);
         griddep_wait();
         for (int i = 0; i < npre; ++i) {
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[i]);
             if (i >= kUmmaPreWaitStages) {  // the rest of the first ring, after the first token boxes
                 mbar_expect_tx(fb, w_box);
-                tma_load_2d_hint(ring + i * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb, w_policy);
+                load_w(i, ring + i * a.stage_bytes, fb);
             }
             mbar_arrive_expect_tx(fb, a.x_box_bytes);
-            tma_load_2d(ring + i * a.stage_bytes + w_box, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
+            load_x(i, ring + i * a.stage_bytes + w_box, fb);
             *issued = i + 1;
         }
-        for (int i = npre; i < nkb; ++i) {
+        for (int i = npre; i < nst; ++i) {
             const int slot = i % a.ring_stages;
             const uint32_t par = static_cast<uint32_t>((i / a.ring_stages) - 1) & 1u;
             if (!umma_wait(smem_u32(&empty[slot]), par, a.wait_limit_ns, abort_flag)) {
@@ -184,8 +199,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
             if (i == a.skip_stage) continue;
             const uint32_t fb = smem_u32(&full[slot]);
             mbar_arrive_expect_tx(fb, a.stage_bytes);
-            tma_load_2d_hint(ring + slot * a.stage_bytes, &tmap_w, (kb0 + i) * kBoxK, row0, fb, w_policy);
-            tma_load_2d(ring + slot * a.stage_bytes + w_box, &tmap_x, (kb0 + i) * kBoxK, 0, fb);
+            load_w(i, ring + slot * a.stage_bytes, fb);
+            load_x(i, ring + slot * a.stage_bytes + w_box, fb);
             *issued = i + 1;
         }
     } else if (warp == 1 && lane == 0) {
@@ -195,7 +210,7 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                                | (kFmt << 7) | (kFmt << 10)    // A, B element type
                                | (static_cast<uint32_t>(NT >> 3) << 17)  // N
                                | (static_cast<uint32_t>(TR >> 4) << 24);  // M: the tile's weight rows
-        for (int i = 0; i < nkb; ++i) {
+        for (int i = 0; i < nst; ++i) {
             const int slot = i % a.ring_stages;
             const uint32_t par = static_cast<uint32_t>(i / a.ring_stages) & 1u;
             if (!umma_wait(smem_u32(&full[slot]), par, a.wait_limit_ns, abort_flag)) {
@@ -204,16 +219,20 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t wa = ring + slot * a.stage_bytes;
-            const uint32_t xa = wa + w_box;
+            // k-block g of the stage: the weight slab [TR][128 bytes] at g * TR * 128, the
+            // token slab at w_box + g * x_kb (both 1024-byte aligned)
+            for (int g = 0; g < G; ++g) {
+                const uint32_t wa = ring + slot * a.stage_bytes + static_cast<uint32_t>(g * TR * 128);
+                const uint32_t xa = ring + slot * a.stage_bytes + w_box + g * x_kb;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = umma_desc_sw128(wa + k * 32);
-                const uint64_t bd = umma_desc_sw128(xa + k * 32);
-                if constexpr (COMPUTE == kMmaBf16)
-                    umma_f16(tmem_d, ad, bd, idesc, (i | k) != 0 ? 1u : 0u);
-                else
-                    umma_tf32(tmem_d, ad, bd, idesc, (i | k) != 0 ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t ad = umma_desc_sw128(wa + k * 32);
+                    const uint64_t bd = umma_desc_sw128(xa + k * 32);
+                    if constexpr (COMPUTE == kMmaBf16)
+                        umma_f16(tmem_d, ad, bd, idesc, (i | g | k) != 0 ? 1u : 0u);
+                    else
+                        umma_tf32(tmem_d, ad, bd, idesc, (i | g | k) != 0 ? 1u : 0u);
+                }
             }
             umma_commit(smem_u32(&empty[slot]));
         }

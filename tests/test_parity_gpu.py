@@ -80,12 +80,14 @@ def test_edge_shapes(hsp, dtype, K, splits, M):
     (4096, (300, 100), 12, 4, 2, 16),   # 58 rows per CTA: four 16-row tiles, 4 x 2 lane tiles
     (4096, (300, 100), 24, 4, 4, 16),   # four tiles, 4 x 8 lane tiles
     (4096, (200, 100), 20, 3, 4, 16),   # 43 rows per CTA: three tiles
-    (4096, (300, 100), 40, 2, 8, 16),   # 33-64 tokens: at most two tiles (8 x 8), two waves of CTAs
+    (4096, (300, 100), 40, 3, 8, 16),   # 33-64 tokens: at most three tiles (12 x 8)
+    (4096, (150, 50), 40, 2, 8, 16),    # 29 rows per CTA: two tiles (8 x 8)
+    (4096, (60, 40), 48, 1, 8, 16),     # 15 rows per CTA: one tile (4 x 8)
     (2048, (60, 40), 10, 1, 2, 2),      # one tile, two K slices
 ])
 def test_fp32_chunk_layout_tiles(hsp, K, splits, M, row_tiles, token_tiles, slices):
     """fp32 above 8 tokens: eight K warps, each on one 16-byte chunk of every unit, over
-    one to four 16-row tiles (two at most from 33 tokens).  Every instance the planner can
+    one to four 16-row tiles (three at most from 33 tokens).  Every instance the planner can
     pick, against the oracle, fused and separate."""
     plan = hsp.describe_plan(M, K, sum(splits), 1)
     assert (plan["engine"], plan["k_warps"], plan["row_warps"]) == (0, 8, 1), plan
