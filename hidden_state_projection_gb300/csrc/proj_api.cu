@@ -546,14 +546,13 @@ struct UPlan {
 // K slices and k-blocks per slice depend on (K, dtype) only (the summation order).  The
 // ring is sized so that two CTAs fit on an SM (the next call's CTAs start beside this
 // call's last ones).  The tile height, the MMA's M, does not change any output bit
-// (tested): 128 weight rows, or 64 for 64-token tiles when all the 64-row tiles times the
-// slices fit one wave at two CTAs per SM (pair_ctas).  Measured on GB300 (µs, 128-row /
-// 64-row tiles, 8 slices): qk_indexer M = 64: 13.8 / 12.1 -- its 24 KB stages left a ring
-// of three beside the 35 KB receive buffer, against five 16 KB stages and 17 KB; wq_a++wkv
-// M = 64: 10.8 / 10.2; but M = 9 / 16 / 32: 10.6 / 11.7, 10.7 / 11.7, 11.3 / 11.7 (qk) and
-// 8.9 / 9.8 (wq_a++wkv): there the twice as many CTAs read the tokens twice as often.
-// Four slices with 64-row tiles and one CTA per SM (36 clusters of 4 fill 144 SMs) were
-// slower still: 14.8 - 15.7 µs for qk_indexer at every M.
+// (tested): 64 weight rows when all the 64-row tiles times the slices fit one wave at two
+// CTAs per SM (pair_ctas), else 128.  Measured on GB300 (µs, 128-row / 64-row tiles with
+// two-k-block stages, 8 slices): qk_indexer M = 12 / 16 / 24 / 32: 9.87 / 9.87 / 10.31 /
+// 10.32 -> 9.33 / 9.35 / 9.80 / 9.82, wq_a++wkv M = 16 / 32 7.93 / 8.21 -> 7.47 / 7.71; at
+// 64 tokens 64-row tiles won from the start (qk_indexer 13.8 -> 12.1 with one-k-block
+// stages).  Four slices with 64-row tiles and one CTA per SM (36 clusters of 4 fill 144
+// SMs) were slower: 14.8 - 15.7 µs for qk_indexer at every M.
 void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_ctas, UPlan *p) {
     memset(p, 0, sizeof *p);
     const int64_t row_bytes = static_cast<int64_t>(K) * elem_size(dt);
@@ -571,20 +570,16 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_cta
         p->kb_per_slice = ceil_div(p->kb_total, p->S);
     }
     const int wave = pair_ctas[p->S] > 0 ? pair_ctas[p->S] : pair_ctas[1];
-    // 64-row tiles: at 64 tokens when they fit one wave, and whenever 128-row tiles
-    // would leave more than half of the SMs (pair_ctas[1] / 2 of them) without a CTA.
-    const bool few = ceil_div(n_rows, 128) * p->S * 4 <= pair_ctas[1];
-    p->TR = ((p->NT == 64 || few) && ceil_div(n_rows, 64) * p->S <= wave) ? 64 : 128;
+    p->TR = ceil_div(n_rows, 64) * p->S <= wave ? 64 : 128;
     p->tiles = ceil_div(n_rows, p->TR);
     // Two k-blocks per stage (one 3-D box of weights, 256 contiguous bytes of each row,
-    // and one of tokens) for the 64-row tiles at 64 tokens: measured on GB300, qk_indexer
-    // M = 64 10.95 -> 10.37 us, wq_a++wkv M = 64 8.75 -> 8.21 (at 16-32 tokens with
-    // 128-row tiles it was mixed, qk_indexer M = 32 10.08 -> 10.34).  Only where rows are
-    // whole k-blocks and the slices' and the total k-block counts are even: no stage then
+    // and one of tokens) for the 64-row tiles: measured on GB300, qk_indexer M = 64
+    // 10.95 -> 10.37 us, wq_a++wkv M = 64 8.75 -> 8.21 (with 128-row tiles at 16-32
+    // tokens it was mixed, qk_indexer M = 32 10.08 -> 10.34).  Only where rows are whole
+    // k-blocks and the slices' and the total k-block counts are even: no stage then
     // reaches past its slice or adds a zero-filled k-block, so the products and their
     // order, hence every output bit, are those of one k-block per stage.
-    p->G = (p->TR == 64 && p->NT == 64 && row_bytes % 128 == 0 && p->kb_total % 2 == 0 && p->kb_per_slice % 2 == 0)
-               ? 2 : 1;
+    p->G = (p->TR == 64 && row_bytes % 128 == 0 && p->kb_total % 2 == 0 && p->kb_per_slice % 2 == 0) ? 2 : 1;
     p->x_box = p->G * p->NT * 128;
     p->stage_bytes = p->G * p->TR * 128 + p->x_box;
     // receive buffer of the cluster reduction (dedicated); the staging buffer aliases
@@ -592,12 +587,13 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_cta
     const int red_bytes = p->TR * (p->NT + 4) * 4;
     const int recv_bytes = p->S > 1 ? red_bytes : 0;
     int ring = (kUmmaSmemBudget - recv_bytes) / p->stage_bytes;
-    // 64-row tiles at 64 tokens: four stages rather than the five that fit (measured on
-    // GB300, qk_indexer M = 33 / 48 / 64 10.99 / 10.98 / 11.18 -> 10.69 / 10.70 / 10.92 us,
-    // wq_a++wkv M = 64 8.93 -> 8.71; three stages gained less).  The ring depth does not
+    // 64-row tiles: four k-blocks in flight (four one-k-block stages or two of two)
+    // rather than all that fit (measured on GB300 with one-k-block stages, qk_indexer
+    // M = 33 / 48 / 64 10.99 / 10.98 / 11.18 -> 10.69 / 10.70 / 10.92 us, wq_a++wkv M = 64
+    // 8.93 -> 8.71; with two-k-block stages at 16 / 32 tokens, two stages against the four
+    // or five that fit: qk_indexer 10.29 / 10.03 -> 9.35 / 9.82).  The ring depth does not
     // change any output bit.
-    // (four one-k-block stages, or two of two k-blocks: 64 KB in flight either way)
-    if (p->TR == 64 && p->NT == 64 && ring > 4 / p->G) ring = 4 / p->G;
+    if (p->TR == 64 && ring > 4 / p->G) ring = 4 / p->G;
     if (ring < 2) ring = 2;
     const int stages = p->kb_per_slice / p->G;
     if (ring > stages) ring = stages < 2 ? 2 : stages;

@@ -136,10 +136,9 @@ def test_plan_fits_the_hardware(hsp):
                         assert p["rows_per_cta"] in (64, 128) and p["threads"] == 128
                         assert p["smem_bytes"] <= 113 * 1024
                         assert p["ring_stages"] >= 2 and p["rows_per_cta"] % p["slices"] == 0
-                        if p["rows_per_cta"] == 64:  # all 64-row tiles in one wave at 2 per SM, and
-                            # 64 tokens, or 128-row tiles would leave most SMs idle
-                            assert M > 32 or -(-n // 128) * p["slices"] * 4 <= 304
-                            assert -(-n // 64) * p["slices"] <= {1: 304, 2: 304, 4: 296, 8: 288, 16: 224}[p["slices"]]
+                        # 64-row tiles exactly when all of them fit one wave at 2 per SM
+                        fits = -(-n // 64) * p["slices"] <= {1: 304, 2: 304, 4: 296, 8: 288, 16: 224}[p["slices"]]
+                        assert (p["rows_per_cta"] == 64) == fits
 
 
 
