@@ -40,6 +40,7 @@ using hsp::StreamArgs;
 
 constexpr int kSmemLimit = 232448;          // per-block dynamic shared memory on sm_103
 constexpr int kUmmaSmemBudget = 110 * 1024;  // tensor-memory kernel: ring + receive buffer, two CTAs per SM
+constexpr int kUmmaTrioSmemBudget = 74 * 1024;  // the same at three CTAs per SM
 constexpr int kSmemReserve = 1024 + 1024;   // ring alignment slack (1024 for the swizzle) + barriers + flags
 constexpr int kStageWeightBytes = 65536;    // tensor layout: weight bytes per ring stage
 constexpr int kMaxRingStages = 32;
@@ -101,6 +102,7 @@ struct DeviceInfo {
     int *err_word = nullptr;
     int cluster_ctas[17] = {0};  // CTAs co-resident in clusters of 1, 2, 4, 8, 16 (index = size)
     int pair_ctas[17] = {0};     // the same at two CTAs per SM (the tensor-memory kernel's footprint)
+    int trio_ctas[17] = {0};     // and at three (its 64-row tiles at 9-32 tokens)
 };
 
 // Stand-in kernel for the co-residency query.  Default shape: the streaming kernels,
@@ -199,8 +201,10 @@ proj_status device_info(DeviceInfo *out) {
             d.cluster_ctas[4] = co_resident_ctas(4, d.sms);
             d.cluster_ctas[8] = co_resident_ctas(8, d.sms * 3 / 4);
             d.cluster_ctas[16] = co_resident_ctas(16, d.sms * 2 / 3);
-            for (int c = 1; c <= 16; c *= 2)
+            for (int c = 1; c <= 16; c *= 2) {
                 d.pair_ctas[c] = co_resident_ctas(c, d.cluster_ctas[c], hsp::kUmmaThreadsHost, kUmmaSmemBudget);
+                d.trio_ctas[c] = co_resident_ctas(c, d.pair_ctas[c], hsp::kUmmaThreadsHost, kUmmaTrioSmemBudget);
+            }
             void *p = nullptr;
             if ((e = cudaGetSymbolAddress(&p, g_hsp_device_error)) != cudaSuccess)
                 return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
@@ -547,13 +551,16 @@ struct UPlan {
 // ring is sized so that two CTAs fit on an SM (the next call's CTAs start beside this
 // call's last ones).  The tile height, the MMA's M, does not change any output bit
 // (tested): 64 weight rows when all the 64-row tiles times the slices fit one wave at two
-// CTAs per SM (pair_ctas), else 128.  Measured on GB300 (µs, 128-row / 64-row tiles with
+// CTAs per SM (pair_ctas), or at three when the 64-row plan's shared memory allows three
+// (trio_ctas: 16 or 32 tokens; measured on GB300, glm_fused_a 2752 x 6144 at M = 9 / 16 /
+// 32 9.61 / 9.60 / 9.97 -> 8.88 / 8.90 / 9.34 us, the 2784-row cell at M = 16 9.79 ->
+// 9.08), else 128.  Measured on GB300 (µs, 128-row / 64-row tiles with
 // two-k-block stages, 8 slices): qk_indexer M = 12 / 16 / 24 / 32: 9.87 / 9.87 / 10.31 /
 // 10.32 -> 9.33 / 9.35 / 9.80 / 9.82, wq_a++wkv M = 16 / 32 7.93 / 8.21 -> 7.47 / 7.71; at
 // 64 tokens 64-row tiles won from the start (qk_indexer 13.8 -> 12.1 with one-k-block
 // stages).  Four slices with 64-row tiles and one CTA per SM (36 clusters of 4 fill 144
 // SMs) were slower: 14.8 - 15.7 µs for qk_indexer at every M.
-void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_ctas, UPlan *p) {
+void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_ctas, const int *trio_ctas, UPlan *p) {
     memset(p, 0, sizeof *p);
     const int64_t row_bytes = static_cast<int64_t>(K) * elem_size(dt);
     p->compute = dt == PROJ_BF16 ? hsp::kMmaBf16 : hsp::kMmaTf32;
@@ -569,37 +576,45 @@ void make_umma_plan(int M, int K, int n_rows, proj_dtype dt, const int *pair_cta
         --p->S;
         p->kb_per_slice = ceil_div(p->kb_total, p->S);
     }
-    const int wave = pair_ctas[p->S] > 0 ? pair_ctas[p->S] : pair_ctas[1];
-    p->TR = ceil_div(n_rows, 64) * p->S <= wave ? 64 : 128;
-    p->tiles = ceil_div(n_rows, p->TR);
-    // Two k-blocks per stage (one 3-D box of weights, 256 contiguous bytes of each row,
-    // and one of tokens) for the 64-row tiles: measured on GB300, qk_indexer M = 64
-    // 10.95 -> 10.37 us, wq_a++wkv M = 64 8.75 -> 8.21 (with 128-row tiles at 16-32
-    // tokens it was mixed, qk_indexer M = 32 10.08 -> 10.34).  Only where rows are whole
-    // k-blocks and the slices' and the total k-block counts are even: no stage then
-    // reaches past its slice or adds a zero-filled k-block, so the products and their
-    // order, hence every output bit, are those of one k-block per stage.
-    p->G = (p->TR == 64 && row_bytes % 128 == 0 && p->kb_total % 2 == 0 && p->kb_per_slice % 2 == 0) ? 2 : 1;
-    p->x_box = p->G * p->NT * 128;
-    p->stage_bytes = p->G * p->TR * 128 + p->x_box;
-    // receive buffer of the cluster reduction (dedicated); the staging buffer aliases
-    // the ring.  Two CTAs per SM: ring + receive buffer within ~110 KB.
-    const int red_bytes = p->TR * (p->NT + 4) * 4;
-    const int recv_bytes = p->S > 1 ? red_bytes : 0;
-    int ring = (kUmmaSmemBudget - recv_bytes) / p->stage_bytes;
-    // 64-row tiles: four k-blocks in flight (four one-k-block stages or two of two)
-    // rather than all that fit (measured on GB300 with one-k-block stages, qk_indexer
-    // M = 33 / 48 / 64 10.99 / 10.98 / 11.18 -> 10.69 / 10.70 / 10.92 us, wq_a++wkv M = 64
-    // 8.93 -> 8.71; with two-k-block stages at 16 / 32 tokens, two stages against the four
-    // or five that fit: qk_indexer 10.29 / 10.03 -> 9.35 / 9.82).  The ring depth does not
-    // change any output bit.
-    if (p->TR == 64 && ring > 4 / p->G) ring = 4 / p->G;
-    if (ring < 2) ring = 2;
-    const int stages = p->kb_per_slice / p->G;
-    if (ring > stages) ring = stages < 2 ? 2 : stages;
-    while (p->S > 1 && ring * p->stage_bytes < red_bytes) ++ring;
-    p->ring = ring;
-    p->smem = 1024 + ring * p->stage_bytes + recv_bytes + (2 * ring + 2) * 8 + 16 + 64;
+    const int wave2 = pair_ctas[p->S] > 0 ? pair_ctas[p->S] : pair_ctas[1];
+    const int wave3 = trio_ctas[p->S] > 0 ? trio_ctas[p->S] : wave2;
+    const int tiles64 = ceil_div(n_rows, 64) * p->S;
+    // Stage shape, ring and shared memory for tiles of TR weight rows.
+    auto size_for = [&](int TR) {
+        p->TR = TR;
+        p->tiles = ceil_div(n_rows, p->TR);
+        // Two k-blocks per stage (one 3-D box of weights, 256 contiguous bytes of each row,
+        // and one of tokens) for the 64-row tiles: measured on GB300, qk_indexer M = 64
+        // 10.95 -> 10.37 us, wq_a++wkv M = 64 8.75 -> 8.21 (with 128-row tiles at 16-32
+        // tokens it was mixed, qk_indexer M = 32 10.08 -> 10.34).  Only where rows are whole
+        // k-blocks and the slices' and the total k-block counts are even: no stage then
+        // reaches past its slice or adds a zero-filled k-block, so the products and their
+        // order, hence every output bit, are those of one k-block per stage.
+        p->G = (p->TR == 64 && row_bytes % 128 == 0 && p->kb_total % 2 == 0 && p->kb_per_slice % 2 == 0) ? 2 : 1;
+        p->x_box = p->G * p->NT * 128;
+        p->stage_bytes = p->G * p->TR * 128 + p->x_box;
+        // receive buffer of the cluster reduction (dedicated); the staging buffer aliases
+        // the ring.  Two CTAs per SM: ring + receive buffer within ~110 KB (64-row tiles
+        // at 16 or 32 tokens stay under 74 KB, three per SM).
+        const int red_bytes = p->TR * (p->NT + 4) * 4;
+        const int recv_bytes = p->S > 1 ? red_bytes : 0;
+        int ring = (kUmmaSmemBudget - recv_bytes) / p->stage_bytes;
+        // 64-row tiles: four k-blocks in flight (four one-k-block stages or two of two)
+        // rather than all that fit (measured on GB300 with one-k-block stages, qk_indexer
+        // M = 33 / 48 / 64 10.99 / 10.98 / 11.18 -> 10.69 / 10.70 / 10.92 us, wq_a++wkv M = 64
+        // 8.93 -> 8.71; with two-k-block stages at 16 / 32 tokens, two stages against the four
+        // or five that fit: qk_indexer 10.29 / 10.03 -> 9.35 / 9.82).  The ring depth does not
+        // change any output bit.
+        if (p->TR == 64 && ring > 4 / p->G) ring = 4 / p->G;
+        if (ring < 2) ring = 2;
+        const int stages = p->kb_per_slice / p->G;
+        if (ring > stages) ring = stages < 2 ? 2 : stages;
+        while (p->S > 1 && ring * p->stage_bytes < red_bytes) ++ring;
+        p->ring = ring;
+        p->smem = 1024 + ring * p->stage_bytes + recv_bytes + (2 * ring + 2) * 8 + 16 + 64;
+    };
+    size_for(64);
+    if (tiles64 > wave2 && (p->smem > kUmmaTrioSmemBudget || tiles64 > wave3)) size_for(128);
     proj_plan_info &i = p->info;
     i.bucket = M <= 8 ? 0 : (M <= 32 ? 1 : 2);
     i.compute = p->compute;
@@ -624,7 +639,7 @@ proj_status launch_umma_rows(const DeviceInfo &dev, const void *x, const void *w
                              proj_dtype dt, const hsp::SplitTable &splits, const hsp::PrefetchList &pf,
                              cudaStream_t stream) {
     UPlan p;
-    make_umma_plan(M, K, n_rows, dt, dev.pair_ctas, &p);
+    make_umma_plan(M, K, n_rows, dt, dev.pair_ctas, dev.trio_ctas, &p);
     hsp::UmmaLaunchReq r{};
     const uint32_t boxk = 128u / static_cast<uint32_t>(elem_size(dt));
     proj_status st;
@@ -1007,13 +1022,15 @@ proj_status fused_impl(const void *x, const void *w_cat, const int32_t *n_splits
 // host only.  Without a usable device the plan assumes a GB300: 152 SMs, 152 / 152 /
 // 144 / 120 / 112 CTAs co-resident in clusters of 1 / 2 / 4 / 8 / 16.  Leaves the
 // last error string as it was.
-void plan_ctas(int (&ctas)[17], int (&pairs)[17]) {
+void plan_ctas(int (&ctas)[17], int (&pairs)[17], int (&trios)[17]) {
     // GB300 (152 SMs) as measured by the occupancy query, for hosts without the device
     static const int kGb300[17] = {0, 152, 152, 0, 144, 0, 0, 0, 120, 0, 0, 0, 0, 0, 0, 0, 112};
     static const int kGb300Pairs[17] = {0, 304, 304, 0, 296, 0, 0, 0, 288, 0, 0, 0, 0, 0, 0, 0, 224};
+    static const int kGb300Trios[17] = {0, 456, 456, 0, 448, 0, 0, 0, 432, 0, 0, 0, 0, 0, 0, 0, 336};
     for (int k = 0; k < 17; ++k) {
         ctas[k] = kGb300[k];
         pairs[k] = kGb300Pairs[k];
+        trios[k] = kGb300Trios[k];
     }
     char saved[sizeof g_last_error];
     memcpy(saved, g_last_error, sizeof saved);
@@ -1022,6 +1039,7 @@ void plan_ctas(int (&ctas)[17], int (&pairs)[17]) {
         for (int k = 1; k < 17; ++k) {
             ctas[k] = d.cluster_ctas[k];
             pairs[k] = d.pair_ctas[k];
+            trios[k] = d.trio_ctas[k];
         }
     else
         (void)cudaGetLastError();
@@ -1102,8 +1120,8 @@ extern "C" {
 
 size_t proj_rmsnorm_workspace_bytes(int32_t M, int32_t K, const int32_t *n_splits, int32_t num_splits,
                                     const int32_t *norm_cols, proj_dtype dtype) {
-    int ctas[17], pairs[17];
-    plan_ctas(ctas, pairs);
+    int ctas[17], pairs[17], trios[17];
+    plan_ctas(ctas, pairs, trios);
     NormLayout L;
     if (norm_layout(M, K, n_splits, num_splits, norm_cols, dtype, ctas, &L) != PROJ_OK) return 0;
     return L.bytes;
@@ -1412,11 +1430,11 @@ proj_status proj_describe_plan(int32_t M, int32_t K, int32_t n_rows, proj_dtype 
     proj_status st = check_shape(M, K, n_rows, dtype);
     if (st != PROJ_OK) return st;
     if (M < 1 || n_rows < 1) return fail(PROJ_ERR_UNSUPPORTED_SHAPE, "M and n_rows must be at least 1");
-    int ctas[17], pairs[17];
-    plan_ctas(ctas, pairs);
+    int ctas[17], pairs[17], trios[17];
+    plan_ctas(ctas, pairs, trios);
     if (use_umma(M, dtype)) {
         UPlan u;
-        make_umma_plan(M, K, n_rows, dtype, pairs, &u);
+        make_umma_plan(M, K, n_rows, dtype, pairs, trios, &u);
         *info = u.info;
         return ok();
     }
