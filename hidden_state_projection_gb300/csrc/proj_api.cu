@@ -524,11 +524,13 @@ proj_status encode_map(const void *ptr, uint64_t d0, uint64_t d1, uint32_t box0,
 // ---- tensor-memory plan ----------------------------------------------------
 
 // bf16 with 9 <= M <= 64: the tensor-memory kernel.  Measured on GB300 (µs, streaming /
-// tensor memory): qk_indexer M = 9 / 12 / 16: 10.2 / 10.9, 10.7 / 10.9, 11.0 / 10.9;
-// wq_a++wkv: 8.1 / 8.8, 8.3 / 8.8, 8.5 / 8.8; glm_fused_a (2752 rows): 16.7 / 10.6,
-// 18.0 / 10.6, 18.6 / 10.6 -- its 64-row CTAs over four K slices need 172 CTAs, a second
-// wave.  The tensor-memory kernel has no such cliff, so it takes every M >= 9; option
-// large_m_path 1 / 2 forces one of them.
+// tensor memory with its first 128-row tiles): qk_indexer M = 9 / 12 / 16: 10.2 / 10.9,
+// 10.7 / 10.9, 11.0 / 10.9; wq_a++wkv: 8.1 / 8.8, 8.3 / 8.8, 8.5 / 8.8; glm_fused_a (2752
+// rows): 16.7 / 10.6, 18.0 / 10.6, 18.6 / 10.6 -- the streaming kernel's 64-row CTAs over
+// four K slices need 172 CTAs, a second wave.  The tensor-memory kernel has no such cliff,
+// and its 64-row tiles with two-k-block stages since took qk_indexer M = 12 / 16 to 9.33 /
+// 9.35, wq_a++wkv M = 16 to 7.47 and glm_fused_a M = 9 / 16 to 8.88 / 8.90, so it takes
+// every M >= 9; option large_m_path 1 / 2 forces one of them.
 constexpr int kStreamMaxM = 8;
 // PROJ_TF32 runs the tensor-memory kernel (kind::tf32, the fp32 operands read as tf32)
 // only when large_m_path is 2.  Measured on GB300 (µs, streaming mma.sync / tcgen05 over
