@@ -203,8 +203,9 @@ def test_large_m_engines_match_oracle(hsp, M, forced):
 def test_tensor_memory_tile_height_keeps_the_bits(hsp, M):
     """At 33-64 tokens glm_fused_a's 2752 rows run as 128-row tiles when fused (43 tiles of
     64 over eight K slices would not fit one wave at two CTAs per SM) and each of its
-    splits alone as 64-row tiles: the tile height is the MMA's M and must not change a
-    single output bit (fused = separate), and both agree with the oracle."""
+    splits alone as 64-row tiles: the tile height is the MMA's M, and the stage shape (one
+    k-block per stage at 128 rows, two at 64) is the copy granularity; neither may change
+    a single output bit (fused = separate), and both agree with the oracle."""
     wl = W.WORKLOADS["glm_fused_a"]
     x = W.activation(wl, M)
     w_cat = W.weight_cat(wl)
@@ -212,6 +213,23 @@ def test_tensor_memory_tile_height_keeps_the_bits(hsp, M):
     assert [hsp.describe_plan(M, wl.K, n, 0)["rows_per_cta"] for n in wl.splits] == [64] * len(wl.splits)
     outs = _run_both(hsp, x, w_cat, wl.splits)
     check_close(outs, oracle_outputs(x, w_cat, wl.splits), "bf16", f"glm_fused_a M{M}")
+
+
+@pytest.mark.parametrize("M", [9, 16, 32])
+def test_tensor_memory_stage_shape_keeps_the_bits(hsp, M):
+    """9-32 tokens: 4096 rows of K = 6144 run fused as 128-row tiles with one k-block per
+    stage (64 tiles of 64 rows over eight K slices would not fit one wave even at three
+    CTAs per SM), each 2048-row split alone as 64-row tiles with two k-blocks per stage
+    (one 3-D box of each).  The outputs must be bitwise equal and agree with the oracle."""
+    K, splits = 6144, (2048, 2048)
+    fused_plan = hsp.describe_plan(M, K, sum(splits), 0)
+    split_plan = hsp.describe_plan(M, K, splits[0], 0)
+    assert (fused_plan["rows_per_cta"], fused_plan["k_per_stage"]) == (128, 64), fused_plan
+    assert (split_plan["rows_per_cta"], split_plan["k_per_stage"]) == (64, 128), split_plan
+    x, ws = W.random_case(K, splits, M, "bf16", seed=5100 + M)
+    w_cat = torch.cat(ws, 0)
+    outs = _run_both(hsp, x, w_cat, splits)
+    check_close(outs, oracle_outputs(x, w_cat, splits), "bf16", f"stage shape M{M}")
 
 
 @pytest.mark.parametrize("M", [1, 2])
