@@ -145,6 +145,16 @@ def test_plan_fits_the_hardware(hsp):
                             assert fits2 or (fits3 and p["smem_bytes"] <= 74 * 1024)
                         else:
                             assert not fits2 and (M > 32 or not fits3)
+                        # two k-blocks per stage only where no stage reaches past its slice
+                        # or adds a zero-filled k-block (so the bits are those of one)
+                        esz = 2 if dt == 0 else 4
+                        kb_total = -(-wl.K * esz // 128)
+                        if p["k_per_stage"] == 2 * 128 // esz:
+                            assert p["rows_per_cta"] == 64 and wl.K * esz % 128 == 0
+                            assert kb_total % 2 == 0 and p["units_per_slice"] % 2 == 0
+                            assert p["stages_total"] * 2 == p["units_per_slice"]
+                        else:
+                            assert p["k_per_stage"] == 128 // esz
 
 
 
