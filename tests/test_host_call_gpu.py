@@ -45,6 +45,26 @@ def test_host_call_matches_device_call(hsp, name, M, tf32):
                 assert torch.equal(h, r.cpu()), (name, M, rep)
 
 
+def test_host_call_with_ragged_mapped_outputs(hsp):
+    """Mapped outputs whose sizes are not whole 16-byte chunks (a 1 x 1022-byte split) are
+    stored by the projection straight into host memory: two launches, same bits."""
+    K, splits, M = 5120, (1280, 511), 1
+    x, ws = W.random_case(K, splits, M, "bf16", seed=6100)
+    w = torch.cat(ws, 0).cuda()
+    x_dev = torch.empty((M, K), dtype=w.dtype, device="cuda")
+    outs_dev = [torch.empty((M, n), dtype=w.dtype, device="cuda") for n in splits]
+    outs_host = [torch.full((M, n), float("nan"), dtype=w.dtype).pin_memory() for n in splits]
+    call = hsp.HostCall(x.pin_memory(), w, splits, outs_host, x_dev, outs_dev)
+    before = hsp.launch_count()
+    call()
+    torch.cuda.synchronize()
+    assert hsp.launch_count() == before + 2
+    ref = hsp.fused_gemm(x.cuda(), w, splits)
+    hsp.check_device_error()
+    for h, r in zip(outs_host, ref):
+        assert torch.equal(h, r.cpu())
+
+
 @pytest.mark.parametrize("name,M", [("wq_a_wkv", 8), ("indexer_fp32", 64)])
 def test_host_call_with_pageable_tokens(hsp, name, M):
     """Tokens in pageable memory go through a copy-engine copy; outputs in pageable memory
