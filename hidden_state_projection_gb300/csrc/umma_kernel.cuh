@@ -49,10 +49,12 @@
 namespace hsp {
 
 constexpr int kUmmaThreads = 128;
-// Weight boxes requested before the grid-dependency wait; the rest of the first ring
-// follows the first token boxes after the wait (measured on GB300, graphs of back-to-back
-// calls: the whole ring at entry 10.22 / 10.31 / 11.38 us at qk_indexer M = 16 / 32 / 64,
-// two boxes 9.84 / 10.09 / 11.22; wq_a++wkv M = 16 8.22 -> 7.90).
+// Stages whose weight box is requested before the grid-dependency wait (one or two
+// k-blocks each); the rest of the first ring follows the first token boxes after the wait
+// (measured on GB300 with one-k-block stages, graphs of back-to-back calls: the whole ring
+// at entry 10.22 / 10.31 / 11.38 us at qk_indexer M = 16 / 32 / 64, two stages 9.84 /
+// 10.09 / 11.22; wq_a++wkv M = 16 8.22 -> 7.90).  With two-k-block stages the ring is two
+// stages, so the whole ring goes out before the wait.
 constexpr int kUmmaPreWaitStages = 2;
 
 template <int NT>
@@ -133,8 +135,8 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
         *abort_flag = 0;
         *issued = 0;
         mbar_fence_init();
-        // The producer's first two weight boxes go out before the CTA barrier and the TMEM
-        // allocation: they depend on nothing but the barriers initialised just above.
+        // The producer's first two weight boxes (stages) go out before the CTA barrier and
+        // the TMEM allocation: they depend on nothing but the barriers initialised above.
         tma_prefetch_map(&tmap_w);
         tma_prefetch_map(&tmap_x);
         for (int i = 0; i < min(min(nst, a.ring_stages), kUmmaPreWaitStages); ++i) {
