@@ -54,7 +54,8 @@ constexpr int kUmmaThreads = 128;
 // (measured on GB300 with one-k-block stages, graphs of back-to-back calls: the whole ring
 // at entry 10.22 / 10.31 / 11.38 us at qk_indexer M = 16 / 32 / 64, two stages 9.84 /
 // 10.09 / 11.22; wq_a++wkv M = 16 8.22 -> 7.90).  With two-k-block stages the ring is two
-// stages, so the whole ring goes out before the wait.
+// stages, so the whole ring goes out before the wait (one stage instead: qk_indexer M = 16
+// / 32 / 64 9.36 / 9.67 / 10.38 -> 9.50 / 9.79 / 10.47 us).
 constexpr int kUmmaPreWaitStages = 2;
 
 template <int NT>
